@@ -1,0 +1,376 @@
+"""Benchmark: W4 group-128 weight-only linear on one GB300.
+
+Workload (one step): one decode token (M = 1) through the seven Llama-3.1-8B projections
+(q/o 4096x4096, k/v 1024x4096, gate/up 14336x4096, down 4096x14336) of 32 layers, each
+layer with its own seeded synthetic weights (W ~ N(0, 0.02) with 0.1 % outliers x20,
+asymmetric round-to-nearest quantization, group 128): 224 launches of the decode GEMV
+reading 3.77 GB of packed weights + scales + zeros a step, far more than the 129 MB L2,
+so every step streams from HBM.  The launches of each projection kind are captured in a
+CUDA graph; CUDA events between the graphs time each kind.
+
+Reported: value = algorithmic HBM GB/s of the whole step (bytes of packed weights, f32
+scales, u8 zeros, bf16 x and y), roofline of the dominant kernel against the measured
+copy bandwidth, an end-to-end figure through the public API with host buffers, and the
+CPU oracle's throughput on a bounded sample of the same work.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "W4 g128 linear: HBM GB/s & % of peak at M=1; TFLOP/s & % of peak at M=2048"
+UNIT = "GB/s"
+LAYERS = 32
+GROUP = 128
+WORKLOAD = "llama-3.1-8b decode, 7 projections x 32 layers, W4A16 group 128, M=1"
+
+
+def proj_bytes(n: int, k: int, m: int = 1) -> int:
+    """Algorithmic bytes of one projection: packed codes + f32 scale + u8 zero + x + y."""
+    return n * k // 2 + n * (k // GROUP) * 5 + 2 * m * k + 2 * m * n
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        self.file = tempfile.TemporaryFile(mode="w+")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for name, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        busy = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- oracle leg
+def cpu_oracle_sample(target_s: float = 10.0):
+    """Oracle throughput (GB/s of algorithmic bytes) on a bounded sample of the step:
+    leading rows of each of the seven projections, M = 1, all host cores."""
+    import numpy as np
+
+    import oracle
+    from weight_only_quantized_linear_gb300 import synth
+
+    threads = oracle.max_threads()
+    oracle.set_threads(threads)
+    rng = np.random.default_rng(0)
+    rows = 64
+    done_bytes = 0
+    elapsed = 0.0
+    sampled = []
+    while elapsed < target_s:
+        for name in synth.LLAMA_ORDER:
+            n, k = synth.LLAMA_PROJ[name]
+            packed = rng.integers(0, 256, (rows, k // 2)).astype(np.uint8)
+            scale = (rng.random((rows, k // GROUP)) * 0.01 + 1e-3).astype(np.float32)
+            zero = rng.integers(0, 16, (rows, k // GROUP)).astype(np.uint8)
+            x = synth.normal_bf16((1, k), seed=1).view(__import__("torch").int16).numpy().view(np.uint16)
+            t0 = time.perf_counter()
+            oracle.linear_int4_groups(x, packed, scale, zero, None, rows, GROUP)
+            elapsed += time.perf_counter() - t0
+            done_bytes += rows * k // 2 + rows * (k // GROUP) * 5 + 2 * k + 2 * rows
+            sampled.append(name)
+        rows *= 2
+    return done_bytes / elapsed / 1e9, threads, (
+        f"oracle linear_int4_groups (f64 sums, {threads} threads) on the leading rows of the 7 "
+        f"Llama projections, doubling rows until {target_s:.0f} s: {done_bytes / 1e6:.1f} MB in {elapsed:.1f} s")
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle as it stands, on the host cores, same metric."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    per_step = []
+    info = None
+    for i in range(args.warmup + args.steps):
+        v, threads, sample = cpu_oracle_sample(target_s=2.0)
+        if i >= args.warmup:
+            per_step.append(v)
+        info = (threads, sample)
+    value = statistics.median(per_step)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD + " (bounded CPU sample per step)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": info[0], "kind": "oracle", "sample": info[1]},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------------------- GPU leg
+def build_weights(dev, layers: int, seed0: int = 1000):
+    """Per layer and projection: packed u8 [N, K/2], scale f32 [N, K/G], zero u8 [N, K/G]."""
+    import torch
+
+    import weight_only_quantized_linear_gb300 as wq
+    from weight_only_quantized_linear_gb300 import synth
+
+    weights = []
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    for layer in range(layers):
+        lw = {}
+        for j, name in enumerate(synth.LLAMA_ORDER):
+            n, k = synth.LLAMA_PROJ[name]
+            w = synth.weight_f32(n, k, seed=seed0 + layer * 7 + j, outlier_frac=0.001, device=dev)
+            codes, scale, zero = wq.wq_quantize_groups(w, GROUP, 4, wq.WQ_ASYM, dev_status=st)
+            del w
+            packed = wq.wq_pack_int4(codes, True, dev_status=st)
+            del codes
+            lw[name] = (packed, scale, zero)
+        weights.append(lw)
+    torch.cuda.synchronize()
+    if int(st.item()) != 0:
+        raise RuntimeError(f"quantize/pack device status {int(st.item())}")
+    return weights
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import weight_only_quantized_linear_gb300 as wq
+    from weight_only_quantized_linear_gb300 import synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wq.build()
+    peaks = load_peaks()
+
+    layers = args.layers
+    weights = build_weights(dev, layers, seed0=1000 + 97 * rank)
+    names = synth.LLAMA_ORDER
+    xs = {k: synth.normal_bf16((1, k), seed=5 + k, device="cpu").to(dev) for k in (4096, 14336)}
+    ys = {(l, n): torch.empty((1, synth.LLAMA_PROJ[n][0]), dtype=torch.bfloat16, device=dev)
+          for l in range(layers) for n in names}
+    ws = {}
+    for n in names:
+        N, K = synth.LLAMA_PROJ[n]
+        b = wq.wq_linear_int4_groups_workspace(1, N, K, GROUP)
+        # one workspace per layer and projection: launches never share counters
+        ws[n] = [wq.alloc_workspace(b, dev) for _ in range(layers)]
+    stream = torch.cuda.Stream(device=dev)
+
+    def launch_kind(n):
+        N, K = synth.LLAMA_PROJ[n]
+        for l in range(layers):
+            p, s, z = weights[l][n]
+            wq.wq_linear_int4_groups(xs[K], p, s, z, None, GROUP, y=ys[(l, n)], workspace=ws[n][l], stream=stream)
+
+    # warm the kernels once outside capture (attributes, descriptors), then capture
+    with torch.cuda.stream(stream):
+        for n in names:
+            launch_kind(n)
+    torch.cuda.synchronize()
+    graphs = {}
+    for n in names:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            launch_kind(n)
+        graphs[n] = g
+    torch.cuda.synchronize()
+
+    step_bytes = sum(proj_bytes(*synth.LLAMA_PROJ[n]) for n in names) * layers
+    launches_per_step = len(names) * layers
+
+    def one_step(evs=None):
+        for i, n in enumerate(names):
+            if evs is not None:
+                evs[i].record(stream)
+            graphs[n].replay()
+        if evs is not None:
+            evs[len(names)].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            one_step()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    step_events = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for s in range(args.steps):
+            one_step(step_events[s])
+        t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = step_bytes * world / (ms_per_step * 1e-3) / 1e9
+
+    per_kind_ms = {n: 0.0 for n in names}
+    for evs in step_events:
+        for i, n in enumerate(names):
+            per_kind_ms[n] += evs[i].elapsed_time(evs[i + 1])
+    per_kind = {}
+    for n in names:
+        N, K = synth.LLAMA_PROJ[n]
+        us = per_kind_ms[n] / (args.steps * layers) * 1e3
+        per_kind[n] = {"us_per_launch": round(us, 3), "gbs": round(proj_bytes(N, K) / (us * 1e-6) / 1e9, 1)}
+    dom = max(names, key=lambda n: per_kind_ms[n])
+    dN, dK = synth.LLAMA_PROJ[dom]
+    dom_us = per_kind[dom]["us_per_launch"]
+    achieved = proj_bytes(dN, dK) / (dom_us * 1e-6) / 1e9
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(prof):
+        try:
+            with open(prof) as f:
+                traffic = json.load(f).get(dom)
+        except (OSError, ValueError):
+            traffic = None
+
+    # ---------------- end to end through the public API, host buffers ----------------
+    x_host = {k: v.cpu().pin_memory() for k, v in xs.items()}
+    last = [(layers - 1, n) for n in names]
+    y_host = {key: torch.empty(ys[key].shape, dtype=torch.bfloat16).pin_memory() for key in last}
+    h2d = sum(v.numel() * 2 for v in x_host.values())
+    d2h = sum(v.numel() * 2 for v in y_host.values())
+    e2e_steps = max(3, args.steps)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            for k in xs:
+                xs[k].copy_(x_host[k], non_blocking=True)
+            one_step()
+            for key in last:
+                y_host[key].copy_(ys[key], non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_value = step_bytes * world / (e2e_ms * 1e-3) / 1e9
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        v, threads, sample = cpu_oracle_sample(target_s=args.cpu_seconds)
+        cpu = {"value": round(v, 4), "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 activations, u4 weights, f32 accumulate",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": 1, "group": GROUP, "layers": layers,
+                       "bytes_per_step": step_bytes, "l2": "inputs larger than L2 (3.77 GB of weights a step)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "frac_of_hbm_peak": round(value / world / peaks["hbm_gbs"], 4),
+            "us_per_layer": round(ms_per_step * 1e3 / layers, 3),
+            "per_projection": per_kind,
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+                         "kernel": f"k_gemv<I4G,MT=1> on {dom} {dN}x{dK}",
+                         "bytes_per_launch": proj_bytes(dN, dK), "peak_source": peaks["source"] + " (hbm_gbs)"},
+            "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "how": "public API calls captured in CUDA graphs; pinned x copied in and the last layer's "
+                           "outputs copied out inside the timed region"},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--layers", type=int, default=LAYERS)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

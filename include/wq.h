@@ -1,0 +1,235 @@
+/*
+ * wq.h -- C ABI of libwq: weight-only quantized linear layers y = x . W-hat^T on one
+ * NVIDIA GB300 (sm_103a), with W-hat dequantized on the fly from packed codes and never
+ * expanded to HBM.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [Linnet] "Quantization" (Linnet language docs, std.quant): the format table
+ *            (Int8Linear, Int4Linear, Int4GroupLinear, dequantize_*, linear_int4_groups,
+ *            mxfp4_experts_shared), "Group-wise 4-bit weights", "MXFP4 experts".
+ *   [L8.5]   "Quantization: int8, int4 group (packed), fp8, KV quant" (OpenLearn TinyLLM
+ *            module L8.5): "2. Principles", "3. Worked example by hand".
+ *   [Ch20]   "20. Quantization" (Inference Engineering book): "Symmetric quantization,
+ *            from scratch", "Granularity: who shares a scale", "Packing", "Speed needs
+ *            a kernel".
+ *
+ * Conventions shared by every entry point
+ *   - Every tensor argument is a DEVICE pointer owned by the caller (allocated with
+ *     cudaMalloc / torch).  The library allocates no device memory; scratch space, where
+ *     an operation wants it, is passed in as `workspace`.
+ *   - Row-major, densely packed layouts.  bf16 tensors are passed as `void*` (IEEE
+ *     bfloat16 bit patterns).  Device pointers must be 16-byte aligned.
+ *   - Packed 4-bit data hold two values a byte, the even element in the low nibble
+ *     ([Linnet] "Packed 4-bit formats hold two values a byte, the even element in the
+ *     low nibble"; [L8.5] Packing).
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy default
+ *     stream) and returns a status: argument problems are detected on the host before
+ *     anything is launched, and nothing is launched when the status is not WQ_OK.
+ *   - `dev_status` (nullable, device int32): problems only the device can see are
+ *     OR-ed into it as WQ_DEV_* bits; the caller reads it after synchronizing.  No call
+ *     traps or asserts on the device.
+ *   - No exception crosses this ABI.
+ */
+#ifndef WQ_H_
+#define WQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define WQ_API __attribute__((visibility("default")))
+#else
+#define WQ_API
+#endif
+
+typedef struct CUstream_st* wq_stream_t; /* identical to cudaStream_t */
+
+/* Host-side status codes. */
+enum {
+  WQ_OK = 0,
+  WQ_EINVAL = 1,       /* null pointer, non-positive size, unknown mode */
+  WQ_ESHAPE = 2,       /* sizes break a layout rule (odd width, K % G != 0, ...) */
+  WQ_EALIGN = 3,       /* a pointer is not 16-byte aligned */
+  WQ_ERANGE = 4,       /* a value outside the format's range */
+  WQ_EUNSUPPORTED = 5, /* a valid request this build does not implement */
+  WQ_ECUDA = 6,        /* a CUDA runtime call failed (launch, attribute query) */
+  WQ_EWORKSPACE = 7    /* workspace too small for the chosen launch */
+};
+
+/* Device-side status bits (OR-ed into *dev_status). */
+enum {
+  WQ_DEV_NONFINITE = 1,   /* quantizer saw a non-finite weight or an overflowing range */
+  WQ_DEV_BAD_EXPERT = 2,  /* an expert index outside [0, E); that slot's output is 0 */
+  WQ_DEV_BAD_CODE = 4,    /* pack saw a code outside the 4-bit range; it packed code & 15 */
+  WQ_DEV_TIMEOUT = 8      /* a bounded device wait gave up (results invalid) */
+};
+
+/* Quantizer modes for wq_quantize_groups. */
+enum {
+  WQ_SYM = 0,    /* signed codes in [-Q, Q], Q = 2^(bits-1) - 1, one f32 scale per group */
+  WQ_SYM_U4 = 1, /* as WQ_SYM at 4 bits, stored as code + 8 (u8) with zero = 8 */
+  WQ_ASYM = 2    /* unsigned codes in [0, 2^bits - 1] with an f32 scale and u8 zero */
+};
+
+/* Human-readable name of a WQ_* status. */
+WQ_API const char* wq_status_string(int status);
+
+/* ABI version of this header (major * 100 + minor). */
+WQ_API int wq_version(void);
+
+/* ------------------------------------------------------------------------------------
+ * Group-wise asymmetric 4-bit linear: [Linnet] linear_int4_groups(x, packed, scale,
+ * zero, bias) over the Int4GroupLinear layout, "(q - zero) * scale per group"
+ * (dequantize_int4_groups), "Group-wise 4-bit weights" (the GPTQ / AWQ scheme, 16
+ * levels per group of Group consecutive inputs).
+ *
+ *   y[m, n] = bf16( sum_k x[m, k] * W-hat[n, k] + bias[n] ),
+ *   W-hat[n, k] = bf16( f32(q[n, k] - zero[n, k/G]) * scale[n, k/G] )
+ *
+ *   x       bf16 [M, K]
+ *   packed  u8   [N, K/G, G/2]  (= [N, K/2] row-major; code k of row n is nibble k%2 of
+ *                                byte k/2, unsigned 0..15)
+ *   scale   f32  [N, K/G]
+ *   zero    u8   [N, K/G]       (values 0..15)
+ *   order   must be NULL (act-order input permutation is not implemented:
+ *           WQ_EUNSUPPORTED otherwise)
+ *   bias    bf16 [N] or NULL
+ *   y       bf16 [M, N]         (written; must not alias the inputs)
+ *   group   G in {32, 64, 128, 256}; K % G == 0 (else WQ_ESHAPE)
+ *   workspace / ws_bytes: optional scratch for splitting K across thread blocks.  Size
+ *           it with wq_linear_int4_groups_workspace(); it must be zero-filled once when
+ *           allocated (the kernels leave it zero-filled again on return).  Pass NULL /
+ *           0 to run without cross-block split-K (correct, slower at small N).  Calls
+ *           that share one workspace must not run concurrently on the GPU.
+ * The result is exact up to f32 accumulation order: |y - y_exact| <= 2e-3 *
+ * sum_k |x_k W-hat_k| + 1 bf16 ulp.
+ * ------------------------------------------------------------------------------------ */
+WQ_API int wq_linear_int4_groups(const void* x, int64_t M, int64_t K,
+                                 const uint8_t* packed, const float* scale,
+                                 const uint8_t* zero, const int32_t* order,
+                                 const void* bias, int64_t N, int32_t group, void* y,
+                                 void* workspace, size_t ws_bytes, int32_t* dev_status,
+                                 wq_stream_t stream);
+/* Workspace bytes wq_linear_int4_groups wants for (M, N, K, group) on the current
+ * device (0 if the launch needs none). */
+WQ_API size_t wq_linear_int4_groups_workspace(int64_t M, int64_t N, int64_t K,
+                                              int32_t group);
+
+/* ------------------------------------------------------------------------------------
+ * Symmetric per-row int8 linear: [Linnet] Int8Linear<In, Out, T> (weight [Out, In; i8],
+ * scale [Out; f32], optional bias) with dequantize_int8 "q * scale in f32, cast to T".
+ *   q i8 [N, K]; scale f32 [N]; x bf16 [M, K]; bias bf16 [N] or NULL; y bf16 [M, N].
+ *   K % 16 == 0 (rows start 16-byte aligned).  workspace as for wq_linear_int4_groups,
+ *   sized by wq_linear_rows_workspace().
+ * ------------------------------------------------------------------------------------ */
+WQ_API int wq_linear_int8_rows(const void* x, int64_t M, int64_t K, const int8_t* q,
+                               const float* scale, const void* bias, int64_t N, void* y,
+                               void* workspace, size_t ws_bytes, int32_t* dev_status,
+                               wq_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * Symmetric per-row signed int4 linear: [Linnet] Int4Linear<In, Out, T> (weight
+ * [Out, In/2; i8], scale [Out; f32]) with dequantize_int4 "unpack, then dequantize";
+ * nibbles are 4-bit two's complement ([L8.5] Packing: a nibble v >= 8 means v - 16).
+ *   packed [N, K/2]; scale f32 [N]; K % 32 == 0.  Other arguments as above.
+ * ------------------------------------------------------------------------------------ */
+WQ_API int wq_linear_int4_rows(const void* x, int64_t M, int64_t K, const int8_t* packed,
+                               const float* scale, const void* bias, int64_t N, void* y,
+                               void* workspace, size_t ws_bytes, int32_t* dev_status,
+                               wq_stream_t stream);
+/* Workspace bytes for the two per-row linears (bits = 8 or 4). */
+WQ_API size_t wq_linear_rows_workspace(int64_t M, int64_t N, int64_t K, int32_t bits);
+
+/* ------------------------------------------------------------------------------------
+ * MXFP4 experts, shared input: [Linnet] mxfp4_experts_shared(x, blocks, scales,
+ * experts) -- "a mixture's chosen experts multiplied from MXFP4, each row's slots
+ * sharing one input (x: [R, 1, In])"; dequantize_mxfp4: "E2M1 values in blocks of 32,
+ * one E8M0 scale byte a block"; [L8.5] MXFP4 (element magnitudes 0, .5, 1, 1.5, 2, 3,
+ * 4, 6 times the block's power-of-two scale).
+ *
+ *   y[r, s, n] = bf16( sum_k x[r, k] * W-hat_e[n, k] ),  e = experts[r, s]
+ *   W-hat_e[n, k] = bf16( E2M1(code) * 2^(scales[e, n, k/32] - 127) )
+ *
+ *   x       bf16 [R, 1, K]
+ *   blocks  u8 [E, N, K/32, 16]  (two E2M1 codes a byte, even element low)
+ *   scales  u8 [E, N, K/32]      (E8M0; 255 = NaN)
+ *   experts i32 [R, S]           (an index outside [0, E) gives a zero slot and sets
+ *                                 WQ_DEV_BAD_EXPERT)
+ *   y       bf16 [R, S, N]
+ *   K % 32 == 0.  workspace: sized by wq_mxfp4_experts_shared_workspace(); same rules.
+ * ------------------------------------------------------------------------------------ */
+WQ_API int wq_mxfp4_experts_shared(const void* x, int64_t R, int64_t K,
+                                   const uint8_t* blocks, const uint8_t* scales,
+                                   int64_t E, int64_t N, const int32_t* experts,
+                                   int64_t S, void* y, void* workspace, size_t ws_bytes,
+                                   int32_t* dev_status, wq_stream_t stream);
+WQ_API size_t wq_mxfp4_experts_shared_workspace(int64_t R, int64_t S, int64_t E,
+                                                int64_t N, int64_t K);
+
+/* ------------------------------------------------------------------------------------
+ * Round-to-nearest quantizer, ties to even, one scale per group of `group` consecutive
+ * inputs of a row; the last group of a row may be short ([Ch20] "Symmetric
+ * quantization, from scratch" and "Granularity": scale = max|w| / Q, codes clamped to
+ * [-Q, Q], an all-zero group gets scale 1, a short last group is padded for the
+ * computation; [L8.5] "2. Principles": rint with ties to even, quotients in float32;
+ * [Linnet] "Quantizing a checkpoint": each group rounded to the nearest level).
+ *
+ *   w      f32 [N, K]
+ *   codes  [N, K] one byte a code: i8 for WQ_SYM; u8 for WQ_SYM_U4 and WQ_ASYM
+ *   scale  f32 [N, ceil(K/G)]
+ *   zero   u8  [N, ceil(K/G)] for WQ_SYM_U4 / WQ_ASYM; ignored (may be NULL) for WQ_SYM
+ *   bits   2..8 for WQ_SYM and WQ_ASYM; 4 for WQ_SYM_U4
+ * WQ_SYM: a = max|w|, s = f32(a / Q), code = clamp(rint(f32(w * f32(Q / a))), -Q, Q).
+ * WQ_ASYM: lo = min(0, min w), hi = max(0, max w), L = 2^bits - 1,
+ *   s = f32((hi - lo) / L), r = f32(L / (hi - lo)), zero = clamp(rint(f32(-lo * r)), 0,
+ *   L), code = clamp(rint(f32(w * r)) + zero, 0, L); hi == lo gives s = 1 and
+ *   zero = codes = 2^(bits-1).
+ * When Q / a (or L / (hi - lo)) overflows f32 the codes use the quotient w / s instead.
+ * A group holding a non-finite weight (or whose range overflows f32) is refused: it
+ * gets scale 1 and the code of 0, and WQ_DEV_NONFINITE is set in *dev_status.
+ * ------------------------------------------------------------------------------------ */
+WQ_API int wq_quantize_groups(const float* w, int64_t N, int64_t K, int32_t group,
+                              int32_t bits, int32_t mode, void* codes, float* scale,
+                              uint8_t* zero, int32_t* dev_status, wq_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * Pack / unpack 4-bit codes, two a byte, even column low ([Ch20] Packing; [L8.5]
+ * Packing).  codes [rows, cols] one byte a code (i8 in [-8, 7] when is_unsigned == 0,
+ * u8 in [0, 15] otherwise); packed [rows, cols/2].  cols must be even (WQ_ESHAPE).  A
+ * code outside the range sets WQ_DEV_BAD_CODE (its low nibble is packed).  Unpack
+ * sign-extends when is_unsigned == 0 (a nibble v >= 8 gives v - 16).
+ * ------------------------------------------------------------------------------------ */
+WQ_API int wq_pack_int4(const void* codes, int64_t rows, int64_t cols, int32_t is_unsigned,
+                        uint8_t* packed, int32_t* dev_status, wq_stream_t stream);
+WQ_API int wq_unpack_int4(const uint8_t* packed, int64_t rows, int64_t cols,
+                          int32_t is_unsigned, void* codes, wq_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * Dequantizers ([Linnet] format table: dequantize_int8 "q * scale in f32, cast to T",
+ * dequantize_int4 "unpack, then dequantize", dequantize_int4_groups "(q - zero) *
+ * scale per group", dequantize_mxfp4).  Output bf16, bit-identical to the definitions
+ * above.  These expand W-hat to memory; the linear entry points never do.
+ *   wq_dequantize_int4_groups: packed [N, K/2], scale/zero [N, K/G] -> w [N, K];
+ *                              K % G == 0, G even.
+ *   wq_dequantize_int8_rows:   q i8 [N, K], scale [N] -> w [N, K]
+ *   wq_dequantize_int4_rows:   packed [N, K/2] signed nibbles, scale [N] -> w [N, K]
+ *   wq_dequantize_mxfp4:       blocks [E, N, K/32, 16], scales [E, N, K/32] -> w [E, N, K]
+ * ------------------------------------------------------------------------------------ */
+WQ_API int wq_dequantize_int4_groups(const uint8_t* packed, const float* scale,
+                                     const uint8_t* zero, int64_t N, int64_t K,
+                                     int32_t group, void* w, wq_stream_t stream);
+WQ_API int wq_dequantize_int8_rows(const int8_t* q, const float* scale, int64_t N,
+                                   int64_t K, void* w, wq_stream_t stream);
+WQ_API int wq_dequantize_int4_rows(const int8_t* packed, const float* scale, int64_t N,
+                                   int64_t K, void* w, wq_stream_t stream);
+WQ_API int wq_dequantize_mxfp4(const uint8_t* blocks, const uint8_t* scales, int64_t E,
+                               int64_t N, int64_t K, void* w, wq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* WQ_H_ */

@@ -1,0 +1,354 @@
+// api.cu -- the extern "C" entry points of libwq (declared in include/wq.h).
+//
+// Host side only: argument validation (before anything is launched), the choice of
+// regime (decode GEMV for few activation rows, tcgen05 GEMM for many), TMA descriptor
+// encoding, workspace layout, and the launches on the caller's stream.  No entry point
+// synchronizes, allocates device memory or throws.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "../../include/wq.h"
+#include "common.cuh"
+#include "launch.h"
+
+namespace wq {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+int num_sms_current() {
+  static int cache[kMaxDevices] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return kNumSMsFallback;
+  if (dev < 0 || dev >= kMaxDevices) return kNumSMsFallback;
+  if (cache[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      return kNumSMsFallback;
+    cache[dev] = v;
+  }
+  return cache[dev];
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+
+int run_gemv(Fmt f, const CUtensorMap& map, GemvParams p, int64_t experts_grid,
+             void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  GemvPlan pl = plan_gemv(f, p.M, p.N, p.K, num_sms_current());
+  if (pl.ksplit > 1) {
+    if (workspace == nullptr || ws_bytes == 0) {
+      pl = GemvPlan{1, (int)((p.K + (f == Fmt::I8R ? 511 : 1023)) / (f == Fmt::I8R ? 512 : 1024)),
+                    pl.tiles, 0};
+    } else {
+      if (ws_bytes < pl.ws_bytes) return WQ_EWORKSPACE;
+      if (!aligned(workspace, 256)) return WQ_EALIGN;
+      p.ws_cnt = static_cast<uint32_t*>(workspace);
+      p.ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                           ws_counter_bytes(pl.tiles));
+    }
+  }
+  return launch_gemv(f, map, p, pl, experts_grid, stream) == cudaSuccess ? WQ_OK : WQ_ECUDA;
+}
+
+size_t gemv_ws_bytes(Fmt f, int64_t M, int64_t N, int64_t K) {
+  return plan_gemv(f, M, N, K, num_sms_current()).ws_bytes;
+}
+
+int check_rows_common(const void* x, int64_t M, int64_t K, const void* w, const float* scale,
+                      const void* bias, int64_t N, const void* y) {
+  if (!x || !w || !scale || !y) return WQ_EINVAL;
+  if (M <= 0 || N <= 0 || K <= 0) return WQ_EINVAL;
+  if (M > (1 << 20) || N > (1 << 28) || K > (1 << 28)) return WQ_EUNSUPPORTED;
+  if (!aligned(x, 16) || !aligned(w, 16) || !aligned(scale, 4) || !aligned(y, 2) ||
+      (bias && !aligned(bias, 2)))
+    return WQ_EALIGN;
+  return WQ_OK;
+}
+
+}  // namespace
+
+bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, void* base,
+                          uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
+                          uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_stride_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, dtype, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace wq
+
+using namespace wq;
+
+extern "C" {
+
+WQ_API const char* wq_status_string(int status) {
+  switch (status) {
+    case WQ_OK: return "WQ_OK";
+    case WQ_EINVAL: return "WQ_EINVAL: null pointer, non-positive size or unknown mode";
+    case WQ_ESHAPE: return "WQ_ESHAPE: sizes break a layout rule";
+    case WQ_EALIGN: return "WQ_EALIGN: pointer not aligned";
+    case WQ_ERANGE: return "WQ_ERANGE: value outside the format's range";
+    case WQ_EUNSUPPORTED: return "WQ_EUNSUPPORTED: request not implemented";
+    case WQ_ECUDA: return "WQ_ECUDA: CUDA runtime call failed";
+    case WQ_EWORKSPACE: return "WQ_EWORKSPACE: workspace too small";
+    default: return "unknown wq status";
+  }
+}
+
+WQ_API int wq_version(void) { return 100; }
+
+// ------------------------------------------------------------------ group-wise 4-bit
+WQ_API size_t wq_linear_int4_groups_workspace(int64_t M, int64_t N, int64_t K, int32_t group) {
+  if (M <= 0 || N <= 0 || K <= 0 || group <= 0) return 0;
+  if (M > 16 && gemm_tc_supported(M, N, K, group)) return 0;
+  if (M > 16) return 0;
+  return gemv_ws_bytes(Fmt::I4G, M, N, K);
+}
+
+WQ_API int wq_linear_int4_groups(const void* x, int64_t M, int64_t K, const uint8_t* packed,
+                                 const float* scale, const uint8_t* zero, const int32_t* order,
+                                 const void* bias, int64_t N, int32_t group, void* y,
+                                 void* workspace, size_t ws_bytes, int32_t* dev_status,
+                                 wq_stream_t stream) {
+  if (order != nullptr) return WQ_EUNSUPPORTED;
+  if (!zero) return WQ_EINVAL;
+  int st = check_rows_common(x, M, K, packed, scale, bias, N, y);
+  if (st != WQ_OK) return st;
+  if (group != 32 && group != 64 && group != 128 && group != 256) return WQ_ESHAPE;
+  if (K % group != 0) return WQ_ESHAPE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  if (M > 16 && gemm_tc_supported(M, N, K, group)) {
+    GemmTcParams gp{static_cast<const __nv_bfloat16*>(x), M, N, K, packed, scale, zero, group,
+                    static_cast<const __nv_bfloat16*>(bias), static_cast<__nv_bfloat16*>(y),
+                    dev_status};
+    return launch_gemm_tc(gp, num_sms_current(), s) == cudaSuccess ? WQ_OK : WQ_ECUDA;
+  }
+
+  CUtensorMap map;
+  if (!encode_tensor_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t*>(packed),
+                            (uint64_t)K / 2, (uint64_t)N, (uint64_t)K / 2, 128, 16,
+                            CU_TENSOR_MAP_SWIZZLE_128B))
+    return WQ_ECUDA;
+  GemvParams p{};
+  p.x = static_cast<const __nv_bfloat16*>(x);
+  p.M = M;
+  p.K = K;
+  p.N = N;
+  p.scale = scale;
+  p.zero = zero;
+  p.group = group;
+  p.bias = static_cast<const __nv_bfloat16*>(bias);
+  p.y = static_cast<__nv_bfloat16*>(y);
+  p.dev_status = dev_status;
+  return run_gemv(Fmt::I4G, map, p, 1, M <= 16 ? workspace : nullptr, ws_bytes, s);
+}
+
+// ------------------------------------------------------------------ per-row int8 / int4
+WQ_API size_t wq_linear_rows_workspace(int64_t M, int64_t N, int64_t K, int32_t bits) {
+  if (M <= 0 || N <= 0 || K <= 0 || M > 16) return 0;
+  return gemv_ws_bytes(bits == 8 ? Fmt::I8R : Fmt::I4R, M, N, K);
+}
+
+WQ_API int wq_linear_int8_rows(const void* x, int64_t M, int64_t K, const int8_t* q,
+                               const float* scale, const void* bias, int64_t N, void* y,
+                               void* workspace, size_t ws_bytes, int32_t* dev_status,
+                               wq_stream_t stream) {
+  int st = check_rows_common(x, M, K, q, scale, bias, N, y);
+  if (st != WQ_OK) return st;
+  if (K % 16 != 0) return WQ_ESHAPE;
+  CUtensorMap map;
+  if (!encode_tensor_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<int8_t*>(q),
+                            (uint64_t)K, (uint64_t)N, (uint64_t)K, 128, 16,
+                            CU_TENSOR_MAP_SWIZZLE_128B))
+    return WQ_ECUDA;
+  GemvParams p{};
+  p.x = static_cast<const __nv_bfloat16*>(x);
+  p.M = M;
+  p.K = K;
+  p.N = N;
+  p.scale = scale;
+  p.bias = static_cast<const __nv_bfloat16*>(bias);
+  p.y = static_cast<__nv_bfloat16*>(y);
+  p.dev_status = dev_status;
+  return run_gemv(Fmt::I8R, map, p, 1, M <= 16 ? workspace : nullptr, ws_bytes,
+                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+WQ_API int wq_linear_int4_rows(const void* x, int64_t M, int64_t K, const int8_t* packed,
+                               const float* scale, const void* bias, int64_t N, void* y,
+                               void* workspace, size_t ws_bytes, int32_t* dev_status,
+                               wq_stream_t stream) {
+  int st = check_rows_common(x, M, K, packed, scale, bias, N, y);
+  if (st != WQ_OK) return st;
+  if (K % 32 != 0) return WQ_ESHAPE;
+  CUtensorMap map;
+  if (!encode_tensor_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<int8_t*>(packed),
+                            (uint64_t)K / 2, (uint64_t)N, (uint64_t)K / 2, 128, 16,
+                            CU_TENSOR_MAP_SWIZZLE_128B))
+    return WQ_ECUDA;
+  GemvParams p{};
+  p.x = static_cast<const __nv_bfloat16*>(x);
+  p.M = M;
+  p.K = K;
+  p.N = N;
+  p.scale = scale;
+  p.bias = static_cast<const __nv_bfloat16*>(bias);
+  p.y = static_cast<__nv_bfloat16*>(y);
+  p.dev_status = dev_status;
+  return run_gemv(Fmt::I4R, map, p, 1, M <= 16 ? workspace : nullptr, ws_bytes,
+                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+// ------------------------------------------------------------------ MXFP4 experts
+WQ_API size_t wq_mxfp4_experts_shared_workspace(int64_t R, int64_t S, int64_t E, int64_t N,
+                                                int64_t K) {
+  (void)R; (void)S; (void)E; (void)N; (void)K;
+  return 0;
+}
+
+WQ_API int wq_mxfp4_experts_shared(const void* x, int64_t R, int64_t K, const uint8_t* blocks,
+                                   const uint8_t* scales, int64_t E, int64_t N,
+                                   const int32_t* experts, int64_t S, void* y, void* workspace,
+                                   size_t ws_bytes, int32_t* dev_status, wq_stream_t stream) {
+  (void)workspace; (void)ws_bytes;
+  if (!x || !blocks || !scales || !experts || !y) return WQ_EINVAL;
+  if (R <= 0 || K <= 0 || E <= 0 || N <= 0 || S <= 0) return WQ_EINVAL;
+  if (K % 32 != 0) return WQ_ESHAPE;
+  if (E > 65535 || R * S > (1 << 24) || E * N > (1 << 30)) return WQ_EUNSUPPORTED;
+  if (!aligned(x, 16) || !aligned(blocks, 16) || !aligned(experts, 4) || !aligned(y, 2))
+    return WQ_EALIGN;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  CUtensorMap map;
+  if (!encode_tensor_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t*>(blocks),
+                            (uint64_t)K / 2, (uint64_t)(E * N), (uint64_t)K / 2, 128, 16,
+                            CU_TENSOR_MAP_SWIZZLE_128B))
+    return WQ_ECUDA;
+  // slots whose expert index is out of range are zero-filled by a small kernel
+  if (launch_zero_bad_slots(experts, R * S, E, N, static_cast<__nv_bfloat16*>(y), dev_status,
+                            s) != cudaSuccess)
+    return WQ_ECUDA;
+  GemvParams p{};
+  p.x = static_cast<const __nv_bfloat16*>(x);
+  p.M = R;
+  p.K = K;
+  p.N = N;
+  p.escale = scales;
+  p.experts = experts;
+  p.S = S;
+  p.y = static_cast<__nv_bfloat16*>(y);
+  p.dev_status = dev_status;
+  return run_gemv(Fmt::MXFP4, map, p, E, nullptr, 0, s);
+}
+
+// ------------------------------------------------------------------ quantize / pack
+WQ_API int wq_quantize_groups(const float* w, int64_t N, int64_t K, int32_t group, int32_t bits,
+                              int32_t mode, void* codes, float* scale, uint8_t* zero,
+                              int32_t* dev_status, wq_stream_t stream) {
+  if (!w || !codes || !scale) return WQ_EINVAL;
+  if (N <= 0 || K <= 0 || group <= 0) return WQ_EINVAL;
+  if (mode != WQ_SYM && mode != WQ_SYM_U4 && mode != WQ_ASYM) return WQ_EINVAL;
+  if (mode == WQ_SYM_U4 && bits != 4) return WQ_EINVAL;
+  if (bits < 2 || bits > 8) return WQ_EINVAL;
+  if (mode != WQ_SYM && !zero) return WQ_EINVAL;
+  if (!aligned(w, 4) || !aligned(scale, 4)) return WQ_EALIGN;
+  return launch_quantize(w, N, K, group, bits, mode, codes, scale, zero, dev_status,
+                         reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? WQ_OK
+             : WQ_ECUDA;
+}
+
+WQ_API int wq_pack_int4(const void* codes, int64_t rows, int64_t cols, int32_t is_unsigned,
+                        uint8_t* packed, int32_t* dev_status, wq_stream_t stream) {
+  if (!codes || !packed) return WQ_EINVAL;
+  if (rows <= 0 || cols <= 0) return WQ_EINVAL;
+  if (cols % 2 != 0) return WQ_ESHAPE;
+  return launch_pack(codes, rows, cols, is_unsigned, packed, dev_status,
+                     reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? WQ_OK
+             : WQ_ECUDA;
+}
+
+WQ_API int wq_unpack_int4(const uint8_t* packed, int64_t rows, int64_t cols, int32_t is_unsigned,
+                          void* codes, wq_stream_t stream) {
+  if (!codes || !packed) return WQ_EINVAL;
+  if (rows <= 0 || cols <= 0) return WQ_EINVAL;
+  if (cols % 2 != 0) return WQ_ESHAPE;
+  return launch_unpack(packed, rows, cols, is_unsigned, codes,
+                       reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? WQ_OK
+             : WQ_ECUDA;
+}
+
+// ------------------------------------------------------------------ dequantize exports
+WQ_API int wq_dequantize_int4_groups(const uint8_t* packed, const float* scale,
+                                     const uint8_t* zero, int64_t N, int64_t K, int32_t group,
+                                     void* w, wq_stream_t stream) {
+  if (!packed || !scale || !zero || !w) return WQ_EINVAL;
+  if (N <= 0 || K <= 0 || group <= 0) return WQ_EINVAL;
+  if (group % 2 != 0 || K % group != 0) return WQ_ESHAPE;
+  if (!aligned(scale, 4) || !aligned(w, 2)) return WQ_EALIGN;
+  return launch_dequant_i4g(packed, scale, zero, N, K, group, w,
+                            reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? WQ_OK
+             : WQ_ECUDA;
+}
+
+WQ_API int wq_dequantize_int8_rows(const int8_t* q, const float* scale, int64_t N, int64_t K,
+                                   void* w, wq_stream_t stream) {
+  if (!q || !scale || !w) return WQ_EINVAL;
+  if (N <= 0 || K <= 0) return WQ_EINVAL;
+  if (!aligned(scale, 4) || !aligned(w, 2)) return WQ_EALIGN;
+  return launch_dequant_i8r(q, scale, N, K, w, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? WQ_OK
+             : WQ_ECUDA;
+}
+
+WQ_API int wq_dequantize_int4_rows(const int8_t* packed, const float* scale, int64_t N,
+                                   int64_t K, void* w, wq_stream_t stream) {
+  if (!packed || !scale || !w) return WQ_EINVAL;
+  if (N <= 0 || K <= 0) return WQ_EINVAL;
+  if (K % 2 != 0) return WQ_ESHAPE;
+  if (!aligned(scale, 4) || !aligned(w, 2)) return WQ_EALIGN;
+  return launch_dequant_i4r(packed, scale, N, K, w, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? WQ_OK
+             : WQ_ECUDA;
+}
+
+WQ_API int wq_dequantize_mxfp4(const uint8_t* blocks, const uint8_t* scales, int64_t E,
+                               int64_t N, int64_t K, void* w, wq_stream_t stream) {
+  if (!blocks || !scales || !w) return WQ_EINVAL;
+  if (E <= 0 || N <= 0 || K <= 0) return WQ_EINVAL;
+  if (K % 32 != 0) return WQ_ESHAPE;
+  if (!aligned(w, 2)) return WQ_EALIGN;
+  return launch_dequant_mxfp4(blocks, scales, E, N, K, w,
+                              reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? WQ_OK
+             : WQ_ECUDA;
+}
+
+}  // extern "C"

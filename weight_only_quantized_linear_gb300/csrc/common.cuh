@@ -1,0 +1,254 @@
+// common.cuh -- device helpers shared by the libwq kernels (sm_103a only).
+//
+// Inline PTX for the Blackwell data movers and barriers (mbarrier, cp.async.bulk.tensor),
+// the legacy warp MMA used by the decode GEMV, and the exact nibble -> f32 conversions
+// the dequantizers are built from.  Every wait on a barrier is bounded: it gives up
+// after a deadline on the global timer, and the caller records WQ_DEV_TIMEOUT.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/wq.h"
+
+#if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ < 1000)
+#error "libwq is written for sm_103a (Blackwell) only"
+#endif
+
+namespace wq {
+
+constexpr int kNumSMsFallback = 152;
+// Bounded waits give up after this many nanoseconds of the global timer.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+__host__ __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
+__host__ __device__ __forceinline__ int64_t imax64(int64_t a, int64_t b) { return a > b ? a : b; }
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ------------------------------------------------------------------ mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait until the phase with the given parity has completed.  Returns false if the
+// deadline passed first (the caller must then stop using the barrier's buffers).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// ------------------------------------------------------------------ TMA (bulk tensor)
+// 2-D tile load global -> shared, completing `bytes` on the mbarrier.  Coordinates are
+// in elements of the tensor map (innermost first).  `policy` is an L2 cache policy.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int32_t c0, int32_t c1, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+// L2 policies: streamed weights are read once (evict first); activations are reused.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// ------------------------------------------------------------------ loads
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+// Read-only 16-byte global load that stays in L1 (activations are reused by every
+// thread block of the SM).
+__device__ __forceinline__ uint4 ld_global_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// ------------------------------------------------------------------ warp MMA
+// D(16x8, f32) += A(16x16, bf16, row-major) * B(16x8, bf16, column-major).
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ------------------------------------------------------------------ conversions
+// Pack two f32 into bf16x2 with round-to-nearest-even: `lo` in bits 0..15.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Exact 4-bit dequantization to f32, eight codes of a 32-bit word at a time.
+//
+// Code p of the word (bits 4p..4p+3) is moved into the mantissa of the float 2^23
+// without a shift where it already sits inside the low 20 bits: the float with bits
+// 0x4B000000 | (code << 4p) equals 2^23 + code * 16^p exactly (p <= 4).  Codes 5..7 are
+// first shifted down by 12 bits, landing at multipliers 16^2, 16^3, 16^4.  Subtracting
+// the exact constant 2^23 + zero * m leaves (code - zero) * m exactly, and multiplying
+// by scale / m (an exact power-of-two rescaling of the f32 scale) gives the correctly
+// rounded f32 product (code - zero) * scale: the same real number, rounded once.  The
+// conversion to bf16 then rounds to nearest even.  So every element equals
+// bf16(f32(code - zero) * scale), bit for bit, while costing one logic op, half a
+// packed add, half a packed multiply and half a bf16x2 conversion per element.
+//
+// Multipliers of the four element pairs (0,1) (2,3) (4,5) (6,7) of a word:
+//   (1, 16)  (256, 4096)  (65536, 256)  (4096, 65536)
+struct Nib8Consts {
+  float2 negc[4];  // -(2^23 + zero * m) per pair
+  float2 s[4];     // scale / m per pair
+};
+
+__device__ __forceinline__ Nib8Consts make_nib8_consts(float scale, float zero) {
+  const float T = 8388608.0f;  // 2^23
+  const float c1 = -(T + zero), c16 = -(T + zero * 16.0f), c256 = -(T + zero * 256.0f),
+              c4096 = -(T + zero * 4096.0f), c65536 = -(T + zero * 65536.0f);
+  const float s1 = scale, s16 = scale * 0.0625f, s256 = scale * 0.00390625f,
+              s4096 = scale * 0.000244140625f, s65536 = scale * 0.0000152587890625f;
+  Nib8Consts k;
+  k.negc[0] = make_float2(c1, c16);
+  k.negc[1] = make_float2(c256, c4096);
+  k.negc[2] = make_float2(c65536, c256);
+  k.negc[3] = make_float2(c4096, c65536);
+  k.s[0] = make_float2(s1, s16);
+  k.s[1] = make_float2(s256, s4096);
+  k.s[2] = make_float2(s65536, s256);
+  k.s[3] = make_float2(s4096, s65536);
+  return k;
+}
+
+// out[i] = bf16x2 of elements (2i, 2i+1) of the word.
+__device__ __forceinline__ void dequant_nib8(uint32_t w, const Nib8Consts& k,
+                                             uint32_t (&out)[4]) {
+  const uint32_t t = w >> 12;
+  const uint32_t M = 0x4B000000u;
+  const float2 f01 = make_float2(__uint_as_float(M | (w & 0x0000000Fu)),
+                                 __uint_as_float(M | (w & 0x000000F0u)));
+  const float2 f23 = make_float2(__uint_as_float(M | (w & 0x00000F00u)),
+                                 __uint_as_float(M | (w & 0x0000F000u)));
+  const float2 f45 = make_float2(__uint_as_float(M | (w & 0x000F0000u)),
+                                 __uint_as_float(M | (t & 0x00000F00u)));
+  const float2 f67 = make_float2(__uint_as_float(M | (t & 0x0000F000u)),
+                                 __uint_as_float(M | (t & 0x000F0000u)));
+  const float2 v01 = __fmul2_rn(__fadd2_rn(f01, k.negc[0]), k.s[0]);
+  const float2 v23 = __fmul2_rn(__fadd2_rn(f23, k.negc[1]), k.s[1]);
+  const float2 v45 = __fmul2_rn(__fadd2_rn(f45, k.negc[2]), k.s[2]);
+  const float2 v67 = __fmul2_rn(__fadd2_rn(f67, k.negc[3]), k.s[3]);
+  out[0] = pack_bf16x2(v01.x, v01.y);
+  out[1] = pack_bf16x2(v23.x, v23.y);
+  out[2] = pack_bf16x2(v45.x, v45.y);
+  out[3] = pack_bf16x2(v67.x, v67.y);
+}
+
+// Exact int8 dequantization, four codes of a word: the byte (q + 128) is placed in the
+// mantissa of 2^23 by a byte permute, 2^23 + 128 is subtracted exactly, and the f32
+// product q * scale is rounded once, then to bf16.  out[0] = (b0, b1), out[1] = (b2, b3).
+__device__ __forceinline__ void dequant_i8x4(uint32_t w, float2 negc, float2 s,
+                                             uint32_t (&out)[2]) {
+  const uint32_t u = w ^ 0x80808080u;  // two's complement -> offset binary
+  const uint32_t M = 0x4B000000u;
+  uint32_t b0, b1, b2, b3;
+  asm("prmt.b32 %0, %1, %2, 0x7440;" : "=r"(b0) : "r"(u), "r"(M));
+  asm("prmt.b32 %0, %1, %2, 0x7441;" : "=r"(b1) : "r"(u), "r"(M));
+  asm("prmt.b32 %0, %1, %2, 0x7442;" : "=r"(b2) : "r"(u), "r"(M));
+  asm("prmt.b32 %0, %1, %2, 0x7443;" : "=r"(b3) : "r"(u), "r"(M));
+  const float2 v01 =
+      __fmul2_rn(__fadd2_rn(make_float2(__uint_as_float(b0), __uint_as_float(b1)), negc), s);
+  const float2 v23 =
+      __fmul2_rn(__fadd2_rn(make_float2(__uint_as_float(b2), __uint_as_float(b3)), negc), s);
+  out[0] = pack_bf16x2(v01.x, v01.y);
+  out[1] = pack_bf16x2(v23.x, v23.y);
+}
+
+// E8M0 scale byte -> 2^(b - 127) as f32 (b = 0 is the subnormal 2^-127; 255 is NaN).
+__device__ __forceinline__ float e8m0_to_f32(uint32_t b) {
+  if (b == 255u) return __uint_as_float(0x7FC00000u);
+  if (b == 0u) return __uint_as_float(0x00400000u);
+  return __uint_as_float(b << 23);
+}
+
+// Two E2M1 codes (a byte, even element in the low nibble) -> two f32 values, through
+// the hardware E2M1x2 -> f16x2 conversion (exact: every E2M1 value is an f16).
+__device__ __forceinline__ float2 e2m1x2_to_f32x2(uint32_t byte_in_low_bits) {
+  uint32_t h;
+  asm("{\n .reg .b8 t;\n cvt.u8.u32 t, %1;\n cvt.rn.f16x2.e2m1x2 %0, t;\n}"
+      : "=r"(h)
+      : "r"(byte_in_low_bits));
+  const __half2 hh = *reinterpret_cast<const __half2*>(&h);
+  return __half22float2(hh);
+}
+
+// Eight E2M1 codes of a word times the block scale X -> four bf16x2 (exact products).
+__device__ __forceinline__ void dequant_e2m1x8(uint32_t w, float2 X, uint32_t (&out)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 v = __fmul2_rn(e2m1x2_to_f32x2(w >> (8 * i)), X);
+    out[i] = pack_bf16x2(v.x, v.y);
+  }
+}
+
+__device__ __forceinline__ void set_dev_status(int32_t* st, int32_t bits) {
+  if (st) atomicOr(st, bits);
+}
+
+}  // namespace wq

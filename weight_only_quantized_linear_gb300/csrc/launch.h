@@ -1,0 +1,90 @@
+// launch.h -- internal interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace wq {
+
+// Storage formats of the decode GEMV.
+enum class Fmt { I4G, I4R, I8R, MXFP4 };
+
+struct GemvParams {
+  const __nv_bfloat16* x;  // activations [M, K] (MXFP4: [R, K])
+  int64_t M;               // activation rows (MXFP4: R)
+  int64_t K;
+  int64_t N;               // output columns (rows of one weight matrix)
+  const float* scale;      // I4G [N, K/G]; I4R / I8R [N]
+  const uint8_t* zero;     // I4G [N, K/G]
+  const uint8_t* escale;   // MXFP4 E8M0 scales [E, N, K/32]
+  int32_t group;           // I4G group size
+  const int32_t* experts;  // MXFP4 [R, S]
+  int64_t S;               // MXFP4 slots per row
+  const __nv_bfloat16* bias;
+  __nv_bfloat16* y;        // [M, N] (MXFP4: [R * S, N])
+  float* ws_part;          // split-K partials [ksplit, M, N]
+  uint32_t* ws_cnt;        // split-K arrival counters [tiles]
+  int32_t ksplit;
+  int32_t stages_per_split;
+  int32_t* dev_status;
+};
+
+struct GemvPlan {
+  int ksplit = 1;
+  int stages_per_split = 1;
+  int tiles = 1;
+  size_t ws_bytes = 0;
+};
+
+// Workspace layout of split-K launches: arrival counters (one a tile, zero between calls)
+// rounded up to 256 bytes, then the f32 partial sums [ksplit, M, N].
+inline size_t ws_counter_bytes(int tiles) { return ((size_t)tiles * 4 + 255) & ~size_t(255); }
+
+GemvPlan plan_gemv(Fmt f, int64_t M, int64_t N, int64_t K, int num_sms);
+cudaError_t launch_gemv(Fmt f, const CUtensorMap& map, GemvParams p, const GemvPlan& plan,
+                        int64_t experts_grid, cudaStream_t stream);
+
+// Load-time and test kernels (quant.cu).
+cudaError_t launch_quantize(const float* w, int64_t N, int64_t K, int32_t G, int32_t bits,
+                            int32_t mode, void* codes, float* scale, uint8_t* zero,
+                            int32_t* dev_status, cudaStream_t s);
+cudaError_t launch_pack(const void* codes, int64_t rows, int64_t cols, int32_t is_unsigned,
+                        uint8_t* packed, int32_t* dev_status, cudaStream_t s);
+cudaError_t launch_unpack(const uint8_t* packed, int64_t rows, int64_t cols,
+                          int32_t is_unsigned, void* codes, cudaStream_t s);
+cudaError_t launch_dequant_i4g(const uint8_t* packed, const float* scale, const uint8_t* zero,
+                               int64_t N, int64_t K, int32_t G, void* w, cudaStream_t s);
+cudaError_t launch_dequant_i8r(const int8_t* q, const float* scale, int64_t N, int64_t K,
+                               void* w, cudaStream_t s);
+cudaError_t launch_dequant_i4r(const int8_t* packed, const float* scale, int64_t N, int64_t K,
+                               void* w, cudaStream_t s);
+cudaError_t launch_zero_bad_slots(const int32_t* experts, int64_t slots, int64_t E, int64_t N,
+                                  __nv_bfloat16* y, int32_t* dev_status, cudaStream_t s);
+cudaError_t launch_dequant_mxfp4(const uint8_t* blocks, const uint8_t* scales, int64_t E,
+                                 int64_t N, int64_t K, void* w, cudaStream_t s);
+
+// Large-M tensor-core GEMM (gemm_tc.cu).  Returns cudaErrorNotSupported when the shape
+// is outside what the kernel handles (the caller then uses the GEMV path).
+struct GemmTcParams {
+  const __nv_bfloat16* x;  // [M, K]
+  int64_t M, N, K;
+  const uint8_t* packed;   // [N, K/2]
+  const float* scale;      // [N, K/G]
+  const uint8_t* zero;     // [N, K/G]
+  int32_t group;
+  const __nv_bfloat16* bias;
+  __nv_bfloat16* y;        // [M, N]
+  int32_t* dev_status;
+};
+bool gemm_tc_supported(int64_t M, int64_t N, int64_t K, int32_t group);
+cudaError_t launch_gemm_tc(const GemmTcParams& p, int num_sms, cudaStream_t stream);
+
+// Tensor-map encoding through the driver entry point (no link-time libcuda).
+bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, void* base,
+                          uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
+                          uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz);
+
+}  // namespace wq
