@@ -140,17 +140,20 @@ def run_reference(args):
     if rank != 0:
         return 0
     per_step = []
+    step_s = []
     info = None
     for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
         v, threads, sample = cpu_oracle_sample(target_s=2.0)
         if i >= args.warmup:
             per_step.append(v)
+            step_s.append(time.perf_counter() - t0)
         info = (threads, sample)
     value = statistics.median(per_step)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * statistics.mean(step_s), 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD + " (bounded CPU sample per step)"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": info[0], "kind": "oracle", "sample": info[1]},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -306,7 +309,7 @@ def run_gpu(args):
     y_host = {key: torch.empty(ys[key].shape, dtype=torch.bfloat16).pin_memory() for key in last}
     h2d = sum(v.numel() * 2 for v in x_host.values())
     d2h = sum(v.numel() * 2 for v in y_host.values())
-    e2e_steps = max(3, args.steps)
+    e2e_steps = max(3, min(args.steps, 500))
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -360,8 +363,8 @@ def run_gpu(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--layers", type=int, default=LAYERS)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -74,7 +74,11 @@ CASES = [
     (9, 64, 1024, 32, False),
     (16, 1024, 4096, 128, True),
     (17, 100, 512, 128, False),           # multiple activation batches
-    (40, 48, 1024, 64, True),
+    (40, 48, 1024, 64, True),             # tensor-core regime from here on
+    (32, 256, 256, 32, False),
+    (256, 512, 4096, 128, True),
+    (300, 300, 1056, 32, True),           # K % 64 == 32, ragged M and N
+    (513, 1000, 2048, 256, False),
 ]
 
 
@@ -240,3 +244,37 @@ def test_mxfp4_many_rows_per_expert_and_bad_index(cuda_device):
     assert bad == 2
     assert (y[3, 1].float() == 0).all() and (y[7, 0].float() == 0).all()
     assert_within(y, yr, ad, "mxfp4 many rows")
+
+
+@pytest.mark.parametrize("grid", [1, 3, 7, 64, 151])
+@pytest.mark.parametrize("M", [1, 13])
+def test_stream_k_partitions(cuda_device, monkeypatch, grid, M):
+    """Every block count gives the same answer: tiles cut anywhere by the equal-share
+    ranges are finished from their partials (deterministically)."""
+    d = cuda_device
+    monkeypatch.setenv("WQ_GEMV_GRID", str(grid))
+    N, K, G = 1000, 4096 + 1024, 128
+    packed, scale, zero = make_i4g(N, K, G, seed=grid)
+    x = synth.normal_bf16((M, K), seed=grid + 1)
+    b = synth.normal_bf16((N,), seed=3)
+    y = run_i4g(d, dev(x, d), dev(packed, d), dev(scale, d), dev(zero, d), dev(b, d), G)
+    yr, ad = oracle.linear_int4_groups(bf16_bits(x), packed, scale, zero, bf16_bits(b), N, G)
+    assert_within(y, yr, ad, f"grid={grid} M={M}")
+    y2 = run_i4g(d, dev(x, d), dev(packed, d), dev(scale, d), dev(zero, d), dev(b, d), G)
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+
+
+def test_gemm_matches_gemv_path(cuda_device, monkeypatch):
+    """The tensor-core regime and the decode regime agree (both within the oracle's
+    tolerance); the crossover moves with WQ_GEMM_MIN_M."""
+    d = cuda_device
+    M, N, K, G = 48, 512, 2048, 128
+    packed, scale, zero = make_i4g(N, K, G, seed=77)
+    x = dev(synth.normal_bf16((M, K), seed=78), d)
+    args = (dev(packed, d), dev(scale, d), dev(zero, d))
+    y_tc = run_i4g(d, x, *args, None, G)
+    monkeypatch.setenv("WQ_GEMM_MIN_M", "100000")
+    y_gemv = run_i4g(d, x, *args, None, G)
+    yr, ad = oracle.linear_int4_groups(bf16_bits(x.cpu()), packed, scale, zero, None, N, G)
+    assert_within(y_tc, yr, ad, "tcgen05")
+    assert_within(y_gemv, yr, ad, "gemv")

@@ -49,13 +49,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 
-int run_gemv(Fmt f, const CUtensorMap& map, GemvParams p, int64_t experts_grid,
-             void* workspace, size_t ws_bytes, cudaStream_t stream) {
+int run_gemv(Fmt f, const CUtensorMap& map, GemvParams p, void* workspace, size_t ws_bytes,
+             cudaStream_t stream) {
   GemvPlan pl = plan_gemv(f, p.M, p.N, p.K, num_sms_current());
-  if (pl.ksplit > 1) {
+  if (pl.stream_k) {
     if (workspace == nullptr || ws_bytes == 0) {
-      pl = GemvPlan{1, (int)((p.K + (f == Fmt::I8R ? 511 : 1023)) / (f == Fmt::I8R ? 512 : 1024)),
-                    pl.tiles, 0};
+      pl.stream_k = false;  // whole tiles a block: correct, less evenly balanced
+      pl.ws_bytes = 0;
     } else {
       if (ws_bytes < pl.ws_bytes) return WQ_EWORKSPACE;
       if (!aligned(workspace, 256)) return WQ_EALIGN;
@@ -64,7 +64,7 @@ int run_gemv(Fmt f, const CUtensorMap& map, GemvParams p, int64_t experts_grid,
                                            ws_counter_bytes(pl.tiles));
     }
   }
-  return launch_gemv(f, map, p, pl, experts_grid, stream) == cudaSuccess ? WQ_OK : WQ_ECUDA;
+  return launch_gemv(f, map, p, pl, stream) == cudaSuccess ? WQ_OK : WQ_ECUDA;
 }
 
 size_t gemv_ws_bytes(Fmt f, int64_t M, int64_t N, int64_t K) {
@@ -160,10 +160,11 @@ WQ_API int wq_linear_int4_groups(const void* x, int64_t M, int64_t K, const uint
   p.scale = scale;
   p.zero = zero;
   p.group = group;
+  p.group_shift = __builtin_ctz((unsigned)group);
   p.bias = static_cast<const __nv_bfloat16*>(bias);
   p.y = static_cast<__nv_bfloat16*>(y);
   p.dev_status = dev_status;
-  return run_gemv(Fmt::I4G, map, p, 1, M <= 16 ? workspace : nullptr, ws_bytes, s);
+  return run_gemv(Fmt::I4G, map, p, M <= 16 ? workspace : nullptr, ws_bytes, s);
 }
 
 // ------------------------------------------------------------------ per-row int8 / int4
@@ -193,7 +194,7 @@ WQ_API int wq_linear_int8_rows(const void* x, int64_t M, int64_t K, const int8_t
   p.bias = static_cast<const __nv_bfloat16*>(bias);
   p.y = static_cast<__nv_bfloat16*>(y);
   p.dev_status = dev_status;
-  return run_gemv(Fmt::I8R, map, p, 1, M <= 16 ? workspace : nullptr, ws_bytes,
+  return run_gemv(Fmt::I8R, map, p, M <= 16 ? workspace : nullptr, ws_bytes,
                   reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -218,7 +219,7 @@ WQ_API int wq_linear_int4_rows(const void* x, int64_t M, int64_t K, const int8_t
   p.bias = static_cast<const __nv_bfloat16*>(bias);
   p.y = static_cast<__nv_bfloat16*>(y);
   p.dev_status = dev_status;
-  return run_gemv(Fmt::I4R, map, p, 1, M <= 16 ? workspace : nullptr, ws_bytes,
+  return run_gemv(Fmt::I4R, map, p, M <= 16 ? workspace : nullptr, ws_bytes,
                   reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -237,7 +238,7 @@ WQ_API int wq_mxfp4_experts_shared(const void* x, int64_t R, int64_t K, const ui
   if (!x || !blocks || !scales || !experts || !y) return WQ_EINVAL;
   if (R <= 0 || K <= 0 || E <= 0 || N <= 0 || S <= 0) return WQ_EINVAL;
   if (K % 32 != 0) return WQ_ESHAPE;
-  if (E > 65535 || R * S > (1 << 24) || E * N > (1 << 30)) return WQ_EUNSUPPORTED;
+  if (!gemv_mxfp4_supported(R, S, E) || E * N > (1 << 30)) return WQ_EUNSUPPORTED;
   if (!aligned(x, 16) || !aligned(blocks, 16) || !aligned(experts, 4) || !aligned(y, 2))
     return WQ_EALIGN;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -258,9 +259,10 @@ WQ_API int wq_mxfp4_experts_shared(const void* x, int64_t R, int64_t K, const ui
   p.escale = scales;
   p.experts = experts;
   p.S = S;
+  p.E = E;
   p.y = static_cast<__nv_bfloat16*>(y);
   p.dev_status = dev_status;
-  return run_gemv(Fmt::MXFP4, map, p, E, nullptr, 0, s);
+  return run_gemv(Fmt::MXFP4, map, p, nullptr, 0, s);
 }
 
 // ------------------------------------------------------------------ quantize / pack

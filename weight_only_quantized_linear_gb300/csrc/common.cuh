@@ -161,8 +161,9 @@ struct Nib8Consts {
 
 __device__ __forceinline__ Nib8Consts make_nib8_consts(float scale, float zero) {
   const float T = 8388608.0f;  // 2^23
-  const float c1 = -(T + zero), c16 = -(T + zero * 16.0f), c256 = -(T + zero * 256.0f),
-              c4096 = -(T + zero * 4096.0f), c65536 = -(T + zero * 65536.0f);
+  // zero * m is exact (at most 15 * 2^16), so each constant is exact
+  const float c1 = -(T + zero), c16 = fmaf(zero, -16.0f, -T), c256 = fmaf(zero, -256.0f, -T),
+              c4096 = fmaf(zero, -4096.0f, -T), c65536 = fmaf(zero, -65536.0f, -T);
   const float s1 = scale, s16 = scale * 0.0625f, s256 = scale * 0.00390625f,
               s4096 = scale * 0.000244140625f, s65536 = scale * 0.0000152587890625f;
   Nib8Consts k;
@@ -175,6 +176,12 @@ __device__ __forceinline__ Nib8Consts make_nib8_consts(float scale, float zero) 
   k.s[2] = make_float2(s65536, s256);
   k.s[3] = make_float2(s4096, s65536);
   return k;
+}
+// The same from an integer zero point 0..255 (converted through the 2^23 magic number:
+// a logic op and an add instead of an int-to-float conversion).
+__device__ __forceinline__ Nib8Consts make_nib8_consts_u(float scale, uint32_t zero) {
+  const float zf = __uint_as_float(0x4B000000u | zero) - 8388608.0f;
+  return make_nib8_consts(scale, zf);
 }
 
 // out[i] = bf16x2 of elements (2i, 2i+1) of the word.

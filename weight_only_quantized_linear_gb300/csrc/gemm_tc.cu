@@ -1,17 +1,368 @@
-// gemm_tc.cu -- large-M group-wise 4-bit linear on the tcgen05 tensor cores.
+// gemm_tc.cu -- prefill-regime (many activation rows) group-wise 4-bit linear on the
+// fifth-generation tensor cores.
+//
+// y[m, n] = sum_k x[m, k] * W-hat[n, k], W-hat[n, k] = bf16(f32(q - zero) * scale)
+// ("Quantization" (Linnet docs): linear_int4_groups over Int4GroupLinear; "20.
+// Quantization" (Inference Engineering book), "Speed needs a kernel": at large batch
+// the product becomes compute-bound and dequantization is extra work, so the weights
+// are dequantized once per tile in shared memory and every dequantized weight feeds
+// 256 activation rows).
+//
+// One thread block computes a 256 x 256 tile of y (rows of x by rows of W):
+//   warp 0      TMA producer: the x tile (256 rows x 64 k, 128-byte swizzle) and the
+//               packed weight tile (256 rows x 32 bytes, 32-byte swizzle) of each k step
+//               into a 3-stage ring, completion on an mbarrier;
+//   warp 1      allocates 512 TMEM columns (two 128 x 256 f32 accumulators) and one of
+//               its threads issues tcgen05.mma kind::f16 (bf16 x bf16 -> f32): 2 x 4
+//               MMAs of 128 x 256 x 16 a k step, then tcgen05.commit frees the stage;
+//   warps 2..9  dequantize: thread t owns weight row t, turns its 32 packed bytes into
+//               64 bf16 values exactly (dequant_nib8) and stores them in the canonical
+//               K-major 128-byte-swizzled layout the MMA reads; after the last k step
+//               they read the accumulators back (tcgen05.ld), add the bias, round to
+//               bf16 and store y.
+// Every wait is bounded; a timeout records WQ_DEV_TIMEOUT and the block winds down
+// after the MMAs it issued have completed, freeing its TMEM.
+#include <atomic>
+#include <cstdlib>
+
 #include "common.cuh"
 #include "launch.h"
 
 namespace wq {
 
+namespace {
+
+constexpr int kBM = 256;  // activation rows a tile (two 128-row accumulators)
+constexpr int kBN = 256;  // weight rows a tile
+constexpr int kBK = 64;   // k a stage: one 128-byte swizzle row of bf16
+constexpr int kStagesTc = 3;
+constexpr int kABytes = kBM * kBK * 2;    // 32 KB
+constexpr int kBBytes = kBN * kBK * 2;    // 32 KB
+constexpr int kPBytes = kBN * kBK / 2;    // 8 KB packed codes
+constexpr int kStageTcBytes = kABytes + kBBytes + kPBytes;
+constexpr int kDequantWarps = 8;
+constexpr int kThreadsTc = (2 + kDequantWarps) * 32;
+constexpr uint32_t kTmemCols = 512;
+
+// ---- tcgen05 ----
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Generic-proxy shared-memory writes -> visible to the async proxy (the MMA's reads).
+__device__ __forceinline__ void fence_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (stride byte offset), base 1024-aligned.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);  // start address
+  d |= (uint64_t)1u << 16;                  // leading byte offset (unused when swizzled)
+  d |= (uint64_t)(1024u >> 4) << 32;        // stride byte offset
+  d |= (uint64_t)1u << 46;                  // descriptor version for tcgen05
+  d |= (uint64_t)2u << 61;                  // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on the mbarrier once every MMA this thread issued so far has completed.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+// 32 lanes x 32 consecutive f32 columns of TMEM -> 32 registers a thread.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+struct SharedTc {
+  uint64_t full_tma[kStagesTc];  // x + packed landed
+  uint64_t full_b[kStagesTc];    // dequantized weights written
+  uint64_t empty[kStagesTc];     // MMAs of the stage done
+  uint64_t acc_full;             // all MMAs done
+  uint32_t tmem_base;
+  int abort;
+};
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreadsTc, 1)
+    k_gemm_w4g_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap pmap,
+                  const GemmTcParams p) {
+  extern __shared__ uint8_t smem_dyn[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
+                                             ~uintptr_t(1023));
+  SharedTc* sh = reinterpret_cast<SharedTc*>(smem + kStagesTc * kStageTcBytes);
+  auto stage_a = [&](int s) { return smem + s * kStageTcBytes; };
+  auto stage_b = [&](int s) { return smem + s * kStageTcBytes + kABytes; };
+  auto stage_p = [&](int s) { return smem + s * kStageTcBytes + kABytes + kBBytes; };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t M = p.M, N = p.N, K = p.K;
+  const int64_t m0 = (int64_t)blockIdx.x * kBM;
+  const int64_t n0 = (int64_t)blockIdx.y * kBN;
+  const int nk = (int)((K + kBK - 1) / kBK);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStagesTc; ++s) {
+      mbar_init(&sh->full_tma[s], 1);
+      mbar_init(&sh->full_b[s], kDequantWarps);
+      mbar_init(&sh->empty[s], 1);
+    }
+    mbar_init(&sh->acc_full, 1);
+    fence_mbar_init();
+    sh->abort = 0;
+  }
+  if (warp == 1) tmem_alloc(&sh->tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh->tmem_base;
+
+  if (warp == 0) {
+    // ================= TMA producer =================
+    if (lane == 0) {
+      tma_prefetch_desc(&xmap);
+      tma_prefetch_desc(&pmap);
+      const uint64_t pol = l2_policy_evict_last();  // x and W tiles are re-read by other blocks
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % kStagesTc;
+        if (kb >= kStagesTc && !mbar_wait(&sh->empty[s], ((kb / kStagesTc) - 1) & 1)) {
+          set_dev_status(p.dev_status, WQ_DEV_TIMEOUT);
+          atomicExch(&sh->abort, 1);
+          break;
+        }
+        if (*reinterpret_cast<volatile int*>(&sh->abort)) break;
+        mbar_arrive_expect_tx(&sh->full_tma[s], kABytes + kPBytes);
+        tma_load_2d(stage_a(s), &xmap, &sh->full_tma[s], kb * kBK, (int32_t)m0, pol);
+        tma_load_2d(stage_p(s), &pmap, &sh->full_tma[s], kb * (kBK / 2), (int32_t)n0, pol);
+      }
+    }
+  } else if (warp == 1) {
+    // ================= MMA issuer =================
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(128, kBN);
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % kStagesTc;
+        if (*reinterpret_cast<volatile int*>(&sh->abort)) break;
+        // the x tile (TMA) and the dequantized weights (dequant warps) of this stage
+        if (!mbar_wait(&sh->full_tma[s], (kb / kStagesTc) & 1) ||
+            !mbar_wait(&sh->full_b[s], (kb / kStagesTc) & 1)) {
+          set_dev_status(p.dev_status, WQ_DEV_TIMEOUT);
+          atomicExch(&sh->abort, 1);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a_base = smem_u32(stage_a(s));
+        const uint32_t b_base = smem_u32(stage_b(s));
+#pragma unroll
+        for (int acc = 0; acc < 2; ++acc) {
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            // +32 bytes a 16-element k slice inside the 128-byte swizzled rows
+            const uint64_t ad = umma_desc_sw128(a_base + acc * (128 * 128) + kk * 32);
+            const uint64_t bd = umma_desc_sw128(b_base + kk * 32);
+            umma_bf16(tmem + acc * kBN, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        umma_commit(&sh->empty[s]);  // the stage may be refilled once these MMAs finish
+      }
+      umma_commit(&sh->acc_full);
+    }
+  } else {
+    // ================= dequantize (8 warps), then epilogue =================
+    const int t = threadIdx.x - 64;  // weight row of the tile owned by this thread
+    const int64_t n = imin64(n0 + t, N - 1);
+    const int gshift = __ffs(p.group) - 1;
+    const int64_t gpr = K >> gshift;
+    const bool two_groups = (p.group < kBK);  // group 32: two groups a k step
+
+    struct Meta {
+      float s0, s1;
+      uint32_t z;
+    };
+    auto load_meta = [&](int kb) -> Meta {
+      Meta m{1.0f, 1.0f, 0u};
+      if (kb >= nk) return m;
+      const int64_t g0 = imin64(((int64_t)kb * kBK) >> gshift, gpr - 1);
+      const int64_t g1 = imin64(g0 + 1, gpr - 1);
+      m.s0 = __ldg(&p.scale[n * gpr + g0]);
+      m.z = __ldg(&p.zero[n * gpr + g0]);
+      if (two_groups) {
+        m.s1 = __ldg(&p.scale[n * gpr + g1]);
+        m.z |= (uint32_t)__ldg(&p.zero[n * gpr + g1]) << 8;
+      }
+      return m;
+    };
+    Meta mq0 = load_meta(0), mq1 = load_meta(1);
+
+    const uint32_t prow = (uint32_t)t * 32;  // packed row, 32-byte swizzle
+    const uint32_t pswz = (uint32_t)((t >> 2) & 1);
+    const uint32_t brow = (uint32_t)t * 128;  // dequantized row, 128-byte swizzle
+    const uint32_t bswz = (uint32_t)(t & 7);
+
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % kStagesTc;
+      const Meta m = mq0;
+      mq0 = mq1;
+      mq1 = load_meta(kb + 2);
+      const Nib8Consts k0 = make_nib8_consts_u(m.s0, m.z & 0xFFu);
+      Nib8Consts k1 = k0;
+      if (two_groups) k1 = make_nib8_consts_u(m.s1, (m.z >> 8) & 0xFFu);
+      if (*reinterpret_cast<volatile int*>(&sh->abort)) break;
+      if (!mbar_wait(&sh->full_tma[s], (kb / kStagesTc) & 1)) {
+        set_dev_status(p.dev_status, WQ_DEV_TIMEOUT);
+        atomicExch(&sh->abort, 1);
+        break;
+      }
+      const uint32_t pbase = smem_u32(stage_p(s)) + prow;
+      const uint4 c0 = ld_shared_v4(pbase + ((0u ^ pswz) << 4));
+      const uint4 c1 = ld_shared_v4(pbase + ((1u ^ pswz) << 4));
+      const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+      const uint32_t bbase = smem_u32(stage_b(s)) + brow;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        uint32_t o[4];
+        dequant_nib8(words[w], (w < 4) ? k0 : k1, o);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                         bbase + (((uint32_t)w ^ bswz) << 4)),
+                     "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
+                     : "memory");
+      }
+      fence_async_shared();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh->full_b[s]);
+    }
+
+    // ---- epilogue: TMEM -> registers -> (+ bias) -> bf16 -> y ----
+    if (!mbar_wait(&sh->acc_full, 0)) {
+      set_dev_status(p.dev_status, WQ_DEV_TIMEOUT);
+      atomicExch(&sh->abort, 1);
+    }
+    tc_fence_after();
+    const int q = warp & 3;          // TMEM lane quarter this warp may read
+    const int acc = (warp - 2) >> 2; // accumulator (activation rows 0..127 or 128..255)
+    const int64_t m = m0 + acc * 128 + q * 32 + lane;
+    const bool vec_ok = (N % 8 == 0) && ((reinterpret_cast<uintptr_t>(p.y) & 15) == 0);
+#pragma unroll 1
+    for (int ch = 0; ch < kBN / 32; ++ch) {
+      uint32_t r[32];
+      tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + acc * kBN + ch * 32, r);
+      const int64_t nb = n0 + ch * 32;
+      if (m < M && nb < N) {
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          v[i] = __uint_as_float(r[i]);
+          if (p.bias && nb + i < N) v[i] += __bfloat162float(p.bias[nb + i]);
+        }
+        __nv_bfloat16* dst = p.y + m * N + nb;
+        if (vec_ok && nb + 32 <= N) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint4 o;
+            o.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
+            o.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
+            o.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
+            o.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
+            *reinterpret_cast<uint4*>(dst + 8 * i) = o;
+          }
+        } else {
+          for (int i = 0; i < 32 && nb + i < N; ++i) dst[i] = __float2bfloat16_rn(v[i]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
 bool gemm_tc_supported(int64_t M, int64_t N, int64_t K, int32_t group) {
-  (void)M; (void)N; (void)K; (void)group;
-  return false;
+  if (const char* env = std::getenv("WQ_GEMM_MIN_M")) {  // tuning knob for the crossover
+    if (M < std::atoll(env)) return false;
+  } else if (M < 32) {
+    return false;
+  }
+  return N >= 1 && K >= 32 && K % 32 == 0 && (group == 32 || group == 64 || group == 128 ||
+                                               group == 256) &&
+         K % group == 0 && M <= (int64_t(1) << 31) && N <= (int64_t(1) << 31);
 }
 
 cudaError_t launch_gemm_tc(const GemmTcParams& p, int num_sms, cudaStream_t stream) {
-  (void)p; (void)num_sms; (void)stream;
-  return cudaErrorNotSupported;
+  (void)num_sms;
+  CUtensorMap xmap, pmap;
+  if (!encode_tensor_map_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                            const_cast<__nv_bfloat16*>(p.x), (uint64_t)p.K, (uint64_t)p.M,
+                            (uint64_t)p.K * 2, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  if (!encode_tensor_map_2d(&pmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t*>(p.packed),
+                            (uint64_t)p.K / 2, (uint64_t)p.N, (uint64_t)p.K / 2, kBK / 2, kBN,
+                            CU_TENSOR_MAP_SWIZZLE_32B))
+    return cudaErrorInvalidValue;
+  const size_t smem = 1024 + (size_t)kStagesTc * kStageTcBytes + sizeof(SharedTc);
+  static std::atomic<uint64_t> attr_set{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(attr_set.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(k_gemm_w4g_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_set.fetch_or(bit, std::memory_order_release);
+  }
+  const dim3 grid((unsigned)((p.M + kBM - 1) / kBM), (unsigned)((p.N + kBN - 1) / kBN));
+  k_gemm_w4g_tc<<<grid, kThreadsTc, smem, stream>>>(xmap, pmap, p);
+  return cudaGetLastError();
 }
 
 }  // namespace wq

@@ -21,31 +21,35 @@ struct GemvParams {
   const uint8_t* zero;     // I4G [N, K/G]
   const uint8_t* escale;   // MXFP4 E8M0 scales [E, N, K/32]
   int32_t group;           // I4G group size
+  int32_t group_shift;     // log2(group)
   const int32_t* experts;  // MXFP4 [R, S]
   int64_t S;               // MXFP4 slots per row
+  int64_t E;               // MXFP4 experts
   const __nv_bfloat16* bias;
   __nv_bfloat16* y;        // [M, N] (MXFP4: [R * S, N])
-  float* ws_part;          // split-K partials [ksplit, M, N]
-  uint32_t* ws_cnt;        // split-K arrival counters [tiles]
-  int32_t ksplit;
-  int32_t stages_per_split;
+  float* ws_part;          // stream-K partial tiles [grid, 2, 16 columns, 16 rows]
+  uint32_t* ws_cnt;        // stream-K arrival counters [tiles]
   int32_t* dev_status;
 };
 
 struct GemvPlan {
-  int ksplit = 1;
-  int stages_per_split = 1;
-  int tiles = 1;
+  int grid = 1;           // persistent thread blocks (at most one an SM)
+  int tiles = 1;          // 16-row weight tiles
+  int spt = 1;            // pipeline stages a tile
+  bool stream_k = false;  // equal stage ranges a block; needs a workspace
   size_t ws_bytes = 0;
 };
 
-// Workspace layout of split-K launches: arrival counters (one a tile, zero between calls)
-// rounded up to 256 bytes, then the f32 partial sums [ksplit, M, N].
+// Workspace layout of stream-K launches: arrival counters (one a tile, zero between
+// calls) rounded up to 256 bytes, then the f32 partial tiles [grid, 2, 16, 16].
 inline size_t ws_counter_bytes(int tiles) { return ((size_t)tiles * 4 + 255) & ~size_t(255); }
+inline size_t ws_partial_bytes(int grid) { return (size_t)grid * 2 * 16 * 16 * 4; }
 
 GemvPlan plan_gemv(Fmt f, int64_t M, int64_t N, int64_t K, int num_sms);
 cudaError_t launch_gemv(Fmt f, const CUtensorMap& map, GemvParams p, const GemvPlan& plan,
-                        int64_t experts_grid, cudaStream_t stream);
+                        cudaStream_t stream);
+// MXFP4 routing tables live in shared memory: bounded slot and expert counts.
+bool gemv_mxfp4_supported(int64_t R, int64_t S, int64_t E);
 
 // Load-time and test kernels (quant.cu).
 cudaError_t launch_quantize(const float* w, int64_t N, int64_t K, int32_t G, int32_t bits,
