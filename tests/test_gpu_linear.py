@@ -252,7 +252,7 @@ def test_stream_k_partitions(cuda_device, monkeypatch, grid, M):
     """Every block count gives the same answer: tiles cut anywhere by the equal-share
     ranges are finished from their partials (deterministically)."""
     d = cuda_device
-    monkeypatch.setenv("WQ_GEMV_GRID", str(grid))
+    monkeypatch.setenv("WQ_GEMV_BLOCKS", str(grid))
     N, K, G = 1000, 4096 + 1024, 128
     packed, scale, zero = make_i4g(N, K, G, seed=grid)
     x = synth.normal_bf16((M, K), seed=grid + 1)

@@ -49,12 +49,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 
-int run_gemv(Fmt f, const CUtensorMap& map, GemvParams p, void* workspace, size_t ws_bytes,
-             cudaStream_t stream) {
+int run_gemv(Fmt f, GemvParams p, void* workspace, size_t ws_bytes, cudaStream_t stream) {
   GemvPlan pl = plan_gemv(f, p.M, p.N, p.K, num_sms_current());
   if (pl.stream_k) {
     if (workspace == nullptr || ws_bytes == 0) {
-      pl.stream_k = false;  // whole tiles a block: correct, less evenly balanced
+      pl.stream_k = false;  // whole tiles a warp: correct, less evenly balanced
       pl.ws_bytes = 0;
     } else {
       if (ws_bytes < pl.ws_bytes) return WQ_EWORKSPACE;
@@ -64,7 +63,7 @@ int run_gemv(Fmt f, const CUtensorMap& map, GemvParams p, void* workspace, size_
                                            ws_counter_bytes(pl.tiles));
     }
   }
-  return launch_gemv(f, map, p, pl, stream) == cudaSuccess ? WQ_OK : WQ_ECUDA;
+  return launch_gemv(f, p, pl, stream) == cudaSuccess ? WQ_OK : WQ_ECUDA;
 }
 
 size_t gemv_ws_bytes(Fmt f, int64_t M, int64_t N, int64_t K) {
@@ -147,13 +146,9 @@ WQ_API int wq_linear_int4_groups(const void* x, int64_t M, int64_t K, const uint
     return launch_gemm_tc(gp, num_sms_current(), s) == cudaSuccess ? WQ_OK : WQ_ECUDA;
   }
 
-  CUtensorMap map;
-  if (!encode_tensor_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t*>(packed),
-                            (uint64_t)K / 2, (uint64_t)N, (uint64_t)K / 2, 128, 16,
-                            CU_TENSOR_MAP_SWIZZLE_128B))
-    return WQ_ECUDA;
   GemvParams p{};
   p.x = static_cast<const __nv_bfloat16*>(x);
+  p.w = packed;
   p.M = M;
   p.K = K;
   p.N = N;
@@ -164,7 +159,7 @@ WQ_API int wq_linear_int4_groups(const void* x, int64_t M, int64_t K, const uint
   p.bias = static_cast<const __nv_bfloat16*>(bias);
   p.y = static_cast<__nv_bfloat16*>(y);
   p.dev_status = dev_status;
-  return run_gemv(Fmt::I4G, map, p, M <= 16 ? workspace : nullptr, ws_bytes, s);
+  return run_gemv(Fmt::I4G, p, M <= 16 ? workspace : nullptr, ws_bytes, s);
 }
 
 // ------------------------------------------------------------------ per-row int8 / int4
@@ -180,13 +175,9 @@ WQ_API int wq_linear_int8_rows(const void* x, int64_t M, int64_t K, const int8_t
   int st = check_rows_common(x, M, K, q, scale, bias, N, y);
   if (st != WQ_OK) return st;
   if (K % 16 != 0) return WQ_ESHAPE;
-  CUtensorMap map;
-  if (!encode_tensor_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<int8_t*>(q),
-                            (uint64_t)K, (uint64_t)N, (uint64_t)K, 128, 16,
-                            CU_TENSOR_MAP_SWIZZLE_128B))
-    return WQ_ECUDA;
   GemvParams p{};
   p.x = static_cast<const __nv_bfloat16*>(x);
+  p.w = reinterpret_cast<const uint8_t*>(q);
   p.M = M;
   p.K = K;
   p.N = N;
@@ -194,7 +185,7 @@ WQ_API int wq_linear_int8_rows(const void* x, int64_t M, int64_t K, const int8_t
   p.bias = static_cast<const __nv_bfloat16*>(bias);
   p.y = static_cast<__nv_bfloat16*>(y);
   p.dev_status = dev_status;
-  return run_gemv(Fmt::I8R, map, p, M <= 16 ? workspace : nullptr, ws_bytes,
+  return run_gemv(Fmt::I8R, p, M <= 16 ? workspace : nullptr, ws_bytes,
                   reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -205,13 +196,9 @@ WQ_API int wq_linear_int4_rows(const void* x, int64_t M, int64_t K, const int8_t
   int st = check_rows_common(x, M, K, packed, scale, bias, N, y);
   if (st != WQ_OK) return st;
   if (K % 32 != 0) return WQ_ESHAPE;
-  CUtensorMap map;
-  if (!encode_tensor_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<int8_t*>(packed),
-                            (uint64_t)K / 2, (uint64_t)N, (uint64_t)K / 2, 128, 16,
-                            CU_TENSOR_MAP_SWIZZLE_128B))
-    return WQ_ECUDA;
   GemvParams p{};
   p.x = static_cast<const __nv_bfloat16*>(x);
+  p.w = reinterpret_cast<const uint8_t*>(packed);
   p.M = M;
   p.K = K;
   p.N = N;
@@ -219,7 +206,7 @@ WQ_API int wq_linear_int4_rows(const void* x, int64_t M, int64_t K, const int8_t
   p.bias = static_cast<const __nv_bfloat16*>(bias);
   p.y = static_cast<__nv_bfloat16*>(y);
   p.dev_status = dev_status;
-  return run_gemv(Fmt::I4R, map, p, M <= 16 ? workspace : nullptr, ws_bytes,
+  return run_gemv(Fmt::I4R, p, M <= 16 ? workspace : nullptr, ws_bytes,
                   reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -242,17 +229,13 @@ WQ_API int wq_mxfp4_experts_shared(const void* x, int64_t R, int64_t K, const ui
   if (!aligned(x, 16) || !aligned(blocks, 16) || !aligned(experts, 4) || !aligned(y, 2))
     return WQ_EALIGN;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  CUtensorMap map;
-  if (!encode_tensor_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t*>(blocks),
-                            (uint64_t)K / 2, (uint64_t)(E * N), (uint64_t)K / 2, 128, 16,
-                            CU_TENSOR_MAP_SWIZZLE_128B))
-    return WQ_ECUDA;
   // slots whose expert index is out of range are zero-filled by a small kernel
   if (launch_zero_bad_slots(experts, R * S, E, N, static_cast<__nv_bfloat16*>(y), dev_status,
                             s) != cudaSuccess)
     return WQ_ECUDA;
   GemvParams p{};
   p.x = static_cast<const __nv_bfloat16*>(x);
+  p.w = blocks;
   p.M = R;
   p.K = K;
   p.N = N;
@@ -262,7 +245,7 @@ WQ_API int wq_mxfp4_experts_shared(const void* x, int64_t R, int64_t K, const ui
   p.E = E;
   p.y = static_cast<__nv_bfloat16*>(y);
   p.dev_status = dev_status;
-  return run_gemv(Fmt::MXFP4, map, p, nullptr, 0, s);
+  return run_gemv(Fmt::MXFP4, p, nullptr, 0, s);
 }
 
 // ------------------------------------------------------------------ quantize / pack

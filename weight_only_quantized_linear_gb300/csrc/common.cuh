@@ -119,6 +119,15 @@ __device__ __forceinline__ uint4 ld_global_nc_v4(const void* p) {
   return v;
 }
 
+// Streaming 16-byte global load: read once, so it does not displace L1 lines.
+__device__ __forceinline__ uint4 ld_global_stream_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
 // ------------------------------------------------------------------ warp MMA
 // D(16x8, f32) += A(16x16, bf16, row-major) * B(16x8, bf16, column-major).
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
@@ -131,6 +140,15 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// acc += lo(a) * lo(b) and acc2 += hi(a) * hi(b) for bf16x2 registers a, b: the bf16
+// products are exact in f32 and each add rounds once (mixed-precision FMA, f32 result).
+__device__ __forceinline__ void fma_bf16x2_f32(uint32_t a, uint32_t b, float& acc, float& acc2) {
+  asm("{\n .reg .b16 al, ah, bl, bh;\n mov.b32 {al, ah}, %2;\n mov.b32 {bl, bh}, %3;\n"
+      " fma.rn.f32.bf16 %0, al, bl, %0;\n fma.rn.f32.bf16 %1, ah, bh, %1;\n}"
+      : "+f"(acc), "+f"(acc2)
+      : "r"(a), "r"(b));
+}
+
 // ------------------------------------------------------------------ conversions
 // Pack two f32 into bf16x2 with round-to-nearest-even: `lo` in bits 0..15.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -141,40 +159,32 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 // Exact 4-bit dequantization to f32, eight codes of a 32-bit word at a time.
 //
-// Code p of the word (bits 4p..4p+3) is moved into the mantissa of the float 2^23
-// without a shift where it already sits inside the low 20 bits: the float with bits
-// 0x4B000000 | (code << 4p) equals 2^23 + code * 16^p exactly (p <= 4).  Codes 5..7 are
-// first shifted down by 12 bits, landing at multipliers 16^2, 16^3, 16^4.  Subtracting
-// the exact constant 2^23 + zero * m leaves (code - zero) * m exactly, and multiplying
-// by scale / m (an exact power-of-two rescaling of the f32 scale) gives the correctly
-// rounded f32 product (code - zero) * scale: the same real number, rounded once.  The
-// conversion to bf16 then rounds to nearest even.  So every element equals
-// bf16(f32(code - zero) * scale), bit for bit, while costing one logic op, half a
-// packed add, half a packed multiply and half a bf16x2 conversion per element.
+// Code p of the word (bits 4p..4p+3) is moved into the mantissa of the float 2^23 by a
+// single logic op: the float with bits 0x4B000000 | (code << 4p) equals 2^23 + code * 16^p
+// exactly for p <= 3.  Codes 4..7 are first shifted down by 16 bits, landing on the same
+// multipliers 1, 16, 256, 4096.  Subtracting the exact constant 2^23 + zero * m leaves
+// (code - zero) * m exactly, and multiplying by scale / m (an exact power-of-two rescaling
+// of the f32 scale) gives the correctly rounded f32 product (code - zero) * scale: the same
+// real number, rounded once.  The conversion to bf16 then rounds to nearest even.  So every
+// element equals bf16(f32(code - zero) * scale), bit for bit, for about one logic op, half
+// a packed add, half a packed multiply and half a paired conversion an element.
 //
-// Multipliers of the four element pairs (0,1) (2,3) (4,5) (6,7) of a word:
-//   (1, 16)  (256, 4096)  (65536, 256)  (4096, 65536)
+// Element pairs (0,1) (2,3) (4,5) (6,7) use the multipliers (1, 16) (256, 4096) (1, 16)
+// (256, 4096): two constant pairs a row.  (Exactness needs scale / 4096 to stay a normal
+// f32, i.e. |scale| >= 2^-114 or scale == 0.)
 struct Nib8Consts {
-  float2 negc[4];  // -(2^23 + zero * m) per pair
-  float2 s[4];     // scale / m per pair
+  float2 negc[2];  // -(2^23 + zero * m) for m = (1, 16) and (256, 4096)
+  float2 s[2];     // scale / m
 };
 
 __device__ __forceinline__ Nib8Consts make_nib8_consts(float scale, float zero) {
   const float T = 8388608.0f;  // 2^23
-  // zero * m is exact (at most 15 * 2^16), so each constant is exact
-  const float c1 = -(T + zero), c16 = fmaf(zero, -16.0f, -T), c256 = fmaf(zero, -256.0f, -T),
-              c4096 = fmaf(zero, -4096.0f, -T), c65536 = fmaf(zero, -65536.0f, -T);
-  const float s1 = scale, s16 = scale * 0.0625f, s256 = scale * 0.00390625f,
-              s4096 = scale * 0.000244140625f, s65536 = scale * 0.0000152587890625f;
+  // zero * m is exact (at most 255 * 4096), so each constant is exact
   Nib8Consts k;
-  k.negc[0] = make_float2(c1, c16);
-  k.negc[1] = make_float2(c256, c4096);
-  k.negc[2] = make_float2(c65536, c256);
-  k.negc[3] = make_float2(c4096, c65536);
-  k.s[0] = make_float2(s1, s16);
-  k.s[1] = make_float2(s256, s4096);
-  k.s[2] = make_float2(s65536, s256);
-  k.s[3] = make_float2(s4096, s65536);
+  k.negc[0] = make_float2(-(T + zero), fmaf(zero, -16.0f, -T));
+  k.negc[1] = make_float2(fmaf(zero, -256.0f, -T), fmaf(zero, -4096.0f, -T));
+  k.s[0] = make_float2(scale, scale * 0.0625f);
+  k.s[1] = make_float2(scale * 0.00390625f, scale * 0.000244140625f);
   return k;
 }
 // The same from an integer zero point 0..255 (converted through the 2^23 magic number:
@@ -187,20 +197,16 @@ __device__ __forceinline__ Nib8Consts make_nib8_consts_u(float scale, uint32_t z
 // out[i] = bf16x2 of elements (2i, 2i+1) of the word.
 __device__ __forceinline__ void dequant_nib8(uint32_t w, const Nib8Consts& k,
                                              uint32_t (&out)[4]) {
-  const uint32_t t = w >> 12;
+  const uint32_t t = w >> 16;
   const uint32_t M = 0x4B000000u;
-  const float2 f01 = make_float2(__uint_as_float(M | (w & 0x0000000Fu)),
-                                 __uint_as_float(M | (w & 0x000000F0u)));
-  const float2 f23 = make_float2(__uint_as_float(M | (w & 0x00000F00u)),
-                                 __uint_as_float(M | (w & 0x0000F000u)));
-  const float2 f45 = make_float2(__uint_as_float(M | (w & 0x000F0000u)),
-                                 __uint_as_float(M | (t & 0x00000F00u)));
-  const float2 f67 = make_float2(__uint_as_float(M | (t & 0x0000F000u)),
-                                 __uint_as_float(M | (t & 0x000F0000u)));
+  const float2 f01 = make_float2(__uint_as_float(M | (w & 0x000Fu)), __uint_as_float(M | (w & 0x00F0u)));
+  const float2 f23 = make_float2(__uint_as_float(M | (w & 0x0F00u)), __uint_as_float(M | (w & 0xF000u)));
+  const float2 f45 = make_float2(__uint_as_float(M | (t & 0x000Fu)), __uint_as_float(M | (t & 0x00F0u)));
+  const float2 f67 = make_float2(__uint_as_float(M | (t & 0x0F00u)), __uint_as_float(M | (t & 0xF000u)));
   const float2 v01 = __fmul2_rn(__fadd2_rn(f01, k.negc[0]), k.s[0]);
   const float2 v23 = __fmul2_rn(__fadd2_rn(f23, k.negc[1]), k.s[1]);
-  const float2 v45 = __fmul2_rn(__fadd2_rn(f45, k.negc[2]), k.s[2]);
-  const float2 v67 = __fmul2_rn(__fadd2_rn(f67, k.negc[3]), k.s[3]);
+  const float2 v45 = __fmul2_rn(__fadd2_rn(f45, k.negc[0]), k.s[0]);
+  const float2 v67 = __fmul2_rn(__fadd2_rn(f67, k.negc[1]), k.s[1]);
   out[0] = pack_bf16x2(v01.x, v01.y);
   out[1] = pack_bf16x2(v23.x, v23.y);
   out[2] = pack_bf16x2(v45.x, v45.y);

@@ -14,6 +14,7 @@ enum class Fmt { I4G, I4R, I8R, MXFP4 };
 
 struct GemvParams {
   const __nv_bfloat16* x;  // activations [M, K] (MXFP4: [R, K])
+  const uint8_t* w;        // packed weights / codes, rows of K/2 (int8: K) bytes
   int64_t M;               // activation rows (MXFP4: R)
   int64_t K;
   int64_t N;               // output columns (rows of one weight matrix)
@@ -27,27 +28,25 @@ struct GemvParams {
   int64_t E;               // MXFP4 experts
   const __nv_bfloat16* bias;
   __nv_bfloat16* y;        // [M, N] (MXFP4: [R * S, N])
-  float* ws_part;          // stream-K partial tiles [grid, 2, 16 columns, 16 rows]
+  float* ws_part;          // stream-K partial tiles [warps, 2, M, 16 rows]
   uint32_t* ws_cnt;        // stream-K arrival counters [tiles]
   int32_t* dev_status;
 };
 
 struct GemvPlan {
-  int grid = 1;           // persistent thread blocks (at most one an SM)
+  int grid = 1;           // thread blocks (a few an SM)
   int tiles = 1;          // 16-row weight tiles
-  int spt = 1;            // pipeline stages a tile
-  bool stream_k = false;  // equal stage ranges a block; needs a workspace
+  int spt = 1;            // 64-byte column chunks a tile
+  bool stream_k = false;  // equal chunk ranges a warp; needs a workspace
   size_t ws_bytes = 0;
 };
 
 // Workspace layout of stream-K launches: arrival counters (one a tile, zero between
-// calls) rounded up to 256 bytes, then the f32 partial tiles [grid, 2, 16, 16].
+// calls) rounded up to 256 bytes, then the f32 partial tiles [warps, 2, M, 16].
 inline size_t ws_counter_bytes(int tiles) { return ((size_t)tiles * 4 + 255) & ~size_t(255); }
-inline size_t ws_partial_bytes(int grid) { return (size_t)grid * 2 * 16 * 16 * 4; }
 
 GemvPlan plan_gemv(Fmt f, int64_t M, int64_t N, int64_t K, int num_sms);
-cudaError_t launch_gemv(Fmt f, const CUtensorMap& map, GemvParams p, const GemvPlan& plan,
-                        cudaStream_t stream);
+cudaError_t launch_gemv(Fmt f, GemvParams p, const GemvPlan& plan, cudaStream_t stream);
 // MXFP4 routing tables live in shared memory: bounded slot and expert counts.
 bool gemv_mxfp4_supported(int64_t R, int64_t S, int64_t E);
 
