@@ -120,6 +120,33 @@ WQ_API size_t wq_linear_int4_groups_workspace(int64_t M, int64_t N, int64_t K,
                                               int32_t group);
 
 /* ------------------------------------------------------------------------------------
+ * Allocation-free variant of wq_linear_int4_groups (the source pages have no
+ * counterpart; it exists for callers of this library).
+ *
+ * Some callers cannot call cudaMalloc and so cannot hand in a workspace: for example a
+ * serving loop that forbids device allocation once it has started, or a host program
+ * that owns every byte of device memory through its own pool and exposes no allocator to
+ * plugins.  This entry point takes the same arguments minus the workspace and allocates
+ * nothing: the split-K scratch it needs lives in one static device array of
+ * WQ_NOALLOC_SCRATCH_BYTES inside libwq, which every GPU that loads the library keeps
+ * until the process exits.
+ *   - Shapes whose split-K scratch would exceed that array are refused with
+ *     WQ_EWORKSPACE before anything is launched.
+ *   - The first call on a device looks up the array's device address (once per device,
+ *     with that device current); make that first call before any stream capture.
+ *   - Every call shares the one array: its arrival counters are cleared on the stream
+ *     before each launch, and calls whose executions overlap on the GPU (two streams, or
+ *     two host threads) race on it.  Serialize them.
+ * Results are those of wq_linear_int4_groups.
+ * ------------------------------------------------------------------------------------ */
+#define WQ_NOALLOC_SCRATCH_BYTES (1024u * 1024u)
+WQ_API int wq_linear_int4_groups_noalloc(const void* x, int64_t M, int64_t K,
+                                         const uint8_t* packed, const float* scale,
+                                         const uint8_t* zero, const int32_t* order,
+                                         const void* bias, int64_t N, int32_t group, void* y,
+                                         int32_t* dev_status, wq_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
  * Symmetric per-row int8 linear: [Linnet] Int8Linear<In, Out, T> (weight [Out, In; i8],
  * scale [Out; f32], optional bias) with dequantize_int8 "q * scale in f32, cast to T".
  *   q i8 [N, K]; scale f32 [N]; x bf16 [M, K]; bias bf16 [N] or NULL; y bf16 [M, N].

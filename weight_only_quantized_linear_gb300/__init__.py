@@ -33,6 +33,8 @@ SIGNATURES = {
     "wq_linear_int4_groups": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P, _P, _P, _I64, _I32, _P, _P, _SZ,
                                              _P, _P]),
     "wq_linear_int4_groups_workspace": (_SZ, [_I64, _I64, _I64, _I32]),
+    "wq_linear_int4_groups_noalloc": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P, _P, _P, _I64, _I32, _P,
+                                                     _P, _P]),
     "wq_linear_int8_rows": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P, _I64, _P, _P, _SZ, _P, _P]),
     "wq_linear_int4_rows": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P, _I64, _P, _P, _SZ, _P, _P]),
     "wq_linear_rows_workspace": (_SZ, [_I64, _I64, _I64, _I32]),
@@ -154,6 +156,27 @@ def wq_linear_int4_groups(x, packed, scale, zero, bias=None, group=128, y=None, 
                                      _ptr(bias), N, group, _ptr(y), _ptr(workspace), ws_bytes,
                                      _ptr(dev_status), _stream(stream))
     _check(st, "wq_linear_int4_groups")
+    return y
+
+
+def wq_linear_int4_groups_noalloc(x, packed, scale, zero, bias=None, group=128, y=None, dev_status=None,
+                                  stream=None, order=None):
+    """wq_linear_int4_groups for callers that cannot allocate device memory: no workspace
+    argument; libwq's own static scratch array is used (shared by every call: do not run
+    two of these concurrently on the GPU)."""
+    _need(x, torch.bfloat16, "x", 2)
+    _need(packed, torch.uint8, "packed")
+    _need(scale, torch.float32, "scale")
+    _need(zero, torch.uint8, "zero")
+    _need(bias, torch.bfloat16, "bias")
+    M, K = x.shape
+    N = packed.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    st = lib().wq_linear_int4_groups_noalloc(_ptr(x), M, K, _ptr(packed), _ptr(scale), _ptr(zero),
+                                             _ptr(order), _ptr(bias), N, group, _ptr(y), _ptr(dev_status),
+                                             _stream(stream))
+    _check(st, "wq_linear_int4_groups_noalloc")
     return y
 
 

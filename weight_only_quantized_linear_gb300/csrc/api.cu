@@ -162,6 +162,59 @@ WQ_API int wq_linear_int4_groups(const void* x, int64_t M, int64_t K, const uint
   return run_gemv(Fmt::I4G, p, M <= 16 ? workspace : nullptr, ws_bytes, s);
 }
 
+// ------------------------------------------------------------------ allocation-free variant
+// Scratch for callers that cannot allocate device memory (see wq.h): one static array a
+// GPU, its device address looked up once per device with cudaGetSymbolAddress (the
+// host-side name of the array is only a stand-in and must never reach a kernel).
+static __device__ __align__(256) uint8_t g_noalloc_scratch[WQ_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {nullptr};
+
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return WQ_ECUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return WQ_ECUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return WQ_OK;
+}
+}  // namespace
+
+WQ_API int wq_linear_int4_groups_noalloc(const void* x, int64_t M, int64_t K,
+                                         const uint8_t* packed, const float* scale,
+                                         const uint8_t* zero, const int32_t* order,
+                                         const void* bias, int64_t N, int32_t group, void* y,
+                                         int32_t* dev_status, wq_stream_t stream) {
+  if (order != nullptr) return WQ_EUNSUPPORTED;
+  if (!zero) return WQ_EINVAL;
+  int st = check_rows_common(x, M, K, packed, scale, bias, N, y);
+  if (st != WQ_OK) return st;
+  if (group != 32 && group != 64 && group != 128 && group != 256) return WQ_ESHAPE;
+  if (K % group != 0) return WQ_ESHAPE;
+  const size_t need = wq_linear_int4_groups_workspace(M, N, K, group);
+  if (need == 0)  // this shape runs without scratch
+    return wq_linear_int4_groups(x, M, K, packed, scale, zero, order, bias, N, group, y,
+                                 nullptr, 0, dev_status, stream);
+  if (need > WQ_NOALLOC_SCRATCH_BYTES) return WQ_EWORKSPACE;
+  void* scratch = nullptr;
+  st = noalloc_scratch(&scratch);
+  if (st != WQ_OK) return st;
+  // the arrival counters must start at zero; the array keeps the last call's contents
+  const GemvPlan pl = plan_gemv(Fmt::I4G, M, N, K, num_sms_current());
+  if (cudaMemsetAsync(scratch, 0, ws_counter_bytes(pl.tiles),
+                      reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return WQ_ECUDA;
+  return wq_linear_int4_groups(x, M, K, packed, scale, zero, order, bias, N, group, y, scratch,
+                               need, dev_status, stream);
+}
+
 // ------------------------------------------------------------------ per-row int8 / int4
 WQ_API size_t wq_linear_rows_workspace(int64_t M, int64_t N, int64_t K, int32_t bits) {
   if (M <= 0 || N <= 0 || K <= 0 || M > 16) return 0;
