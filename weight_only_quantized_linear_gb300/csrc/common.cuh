@@ -119,6 +119,11 @@ __device__ __forceinline__ uint4 ld_global_nc_v4(const void* p) {
   return v;
 }
 
+// Bring the line holding p into L1 ahead of its use (no register, no wait).
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 // Streaming 16-byte global load: read once, so it does not displace L1 lines.
 __device__ __forceinline__ uint4 ld_global_stream_v4(const void* p) {
   uint4 v;
@@ -147,6 +152,32 @@ __device__ __forceinline__ void fma_bf16x2_f32(uint32_t a, uint32_t b, float& ac
       " fma.rn.f32.bf16 %0, al, bl, %0;\n fma.rn.f32.bf16 %1, ah, bh, %1;\n}"
       : "+f"(acc), "+f"(acc2)
       : "r"(a), "r"(b));
+}
+
+// acc += half HA of a * half HB of b (0: bits 0..15, 1: bits 16..31), bf16 inputs: the
+// product is exact in f32 and the add rounds once.
+template <int HA, int HB>
+__device__ __forceinline__ void fma_mix(float& acc, uint32_t a, uint32_t b) {
+  if constexpr (HA == 0 && HB == 0)
+    asm("{\n .reg .b16 a0, a1, b0, b1;\n mov.b32 {a0, a1}, %1;\n mov.b32 {b0, b1}, %2;\n"
+        " fma.rn.f32.bf16 %0, a0, b0, %0;\n}" : "+f"(acc) : "r"(a), "r"(b));
+  else if constexpr (HA == 0 && HB == 1)
+    asm("{\n .reg .b16 a0, a1, b0, b1;\n mov.b32 {a0, a1}, %1;\n mov.b32 {b0, b1}, %2;\n"
+        " fma.rn.f32.bf16 %0, a0, b1, %0;\n}" : "+f"(acc) : "r"(a), "r"(b));
+  else if constexpr (HA == 1 && HB == 0)
+    asm("{\n .reg .b16 a0, a1, b0, b1;\n mov.b32 {a0, a1}, %1;\n mov.b32 {b0, b1}, %2;\n"
+        " fma.rn.f32.bf16 %0, a1, b0, %0;\n}" : "+f"(acc) : "r"(a), "r"(b));
+  else
+    asm("{\n .reg .b16 a0, a1, b0, b1;\n mov.b32 {a0, a1}, %1;\n mov.b32 {b0, b1}, %2;\n"
+        " fma.rn.f32.bf16 %0, a1, b1, %0;\n}" : "+f"(acc) : "r"(a), "r"(b));
+}
+
+// Packed bf16 subtraction a - b, rounded to nearest even (exact for the small integers
+// the factored decode subtracts).
+__device__ __forceinline__ uint32_t sub_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
 // ------------------------------------------------------------------ conversions

@@ -27,6 +27,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cstdlib>
+#include <type_traits>
 
 #include "common.cuh"
 #include "launch.h"
@@ -67,6 +68,75 @@ struct Routing {
 __device__ __forceinline__ int64_t warp_begin(int64_t c, int64_t G, int64_t items, int cpt,
                                               bool whole_items) {
   return whole_items ? (c * items / G) * cpt : c * (items * cpt) / G;
+}
+
+// Finish the tiles cut by warp-range boundaries (stream-K launches only).  Each
+// contributing warp adds one to the tile's counter once its partial is out; the one that
+// brings it to the number of contributors adds the partials in warp order, writes y and
+// clears the counter.  Nobody waits on anybody.  W: chunks of the launch; G: warps.
+__device__ __forceinline__ void finish_cut_tiles(const GemvParams& p, int64_t c, int64_t G,
+                                                 int64_t W, int cpt, const int (&pend_tile)[2],
+                                                 int npend, int lane) {
+  const int64_t N = p.N;
+  // range boundary c * W / G of warp c: 32-bit arithmetic when the product fits
+  const bool narrow = (uint64_t)W * (uint64_t)G < (1ull << 32);
+  auto bound = [&](int64_t cc) -> int64_t {
+    return narrow ? (int64_t)((uint32_t)cc * (uint32_t)W / (uint32_t)G) : cc * W / G;
+  };
+  auto owner = [&](int64_t sidx) -> int64_t {
+    int64_t cc = narrow ? (int64_t)((uint32_t)sidx * (uint32_t)G / (uint32_t)W) : sidx * G / W;
+    while (cc + 1 < G && bound(cc + 1) <= sidx) ++cc;
+    while (cc > 0 && bound(cc) > sidx) --cc;
+    return cc;
+  };
+  for (int i = 0; i < npend; ++i) {
+    const int tile = pend_tile[i];
+    // the lanes' partial stores happen before lane 0's fence (warp barrier), and the
+    // fence before its arrival on the counter
+    __syncwarp();
+    if (lane == 0) __threadfence();
+    const int64_t t_beg = (int64_t)tile * cpt;
+    const int64_t c0 = owner(t_beg), c1 = owner(t_beg + cpt - 1);
+    // warps between c0 and c1 whose range is empty (fewer chunks than warps) take no part
+    uint32_t contributors = 0;
+    for (int64_t cc = c0; cc <= c1; ++cc)
+      if (bound(cc) < bound(cc + 1)) ++contributors;
+    int last = 0;
+    if (lane == 0) last = (atomicAdd(&p.ws_cnt[tile], 1u) == contributors - 1u) ? 1 : 0;
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last) {
+      __threadfence();
+      for (int idx = lane; idx < p.M * kRows; idx += 32) {
+        const int m = idx / kRows, row = idx % kRows;
+        // independent loads four at a time, added in warp order
+        float v = 0.0f;
+        for (int64_t cc0 = c0; cc0 <= c1; cc0 += 4) {
+          float part[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int64_t cc = cc0 + q;
+            part[q] = 0.0f;
+            if (cc <= c1) {
+              const int64_t b0 = bound(cc);
+              if (b0 != bound(cc + 1)) {
+                const int sid = (b0 >= t_beg) ? 0 : 1;
+                part[q] = __ldcg(&p.ws_part[((cc * 2 + sid) * p.M + m) * kRows + row]);
+              }
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) v += part[q];
+        }
+        const int64_t n = (int64_t)tile * kRows + row;
+        if (n < N) {
+          if (p.bias) v += __bfloat162float(p.bias[n]);
+          p.y[(int64_t)m * N + n] = __float2bfloat16_rn(v);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) p.ws_cnt[tile] = 0u;
+    }
+  }
 }
 
 }  // namespace
@@ -175,13 +245,15 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM) k_gemv(const GemvParam
   struct Slot {
     uint4 a, b;
     float sa, sb;
-    uint32_t z;  // zero points (I4G) or block scales (MXFP4) of the two rows; bit 16: valid
+    // zero points (I4G) or E8M0 block scales (MXFP4) of rows A and B, each loaded into a
+    // register of its own: combining them here would wait for the loads
+    uint32_t za, zb;
   };
   auto load_slot = [&](const Rows& r, int ch) -> Slot {
     Slot s;
     s.a = s.b = make_uint4(0, 0, 0, 0);
-    s.sa = s.sb = 0.0f;
-    s.z = 0u;
+    s.sa = s.sb = 0.0f;  // MXFP4: sa = 1 marks a piece inside K
+    s.za = s.zb = 0u;
     const int kp = ch * kChunkK + cq * kPiece;
     if (kp < K) {
       const int64_t wstep = 8 * row_bytes, mstep = 8 * gpr;
@@ -191,17 +263,17 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM) k_gemv(const GemvParam
         const int gi = kp >> gshift;
         if (r.valid & 1u) {
           s.sa = __ldg(r.s + gi);
-          s.z = (uint32_t)__ldg(r.z + gi);
+          s.za = (uint32_t)__ldg(r.z + gi);
         }
         if (r.valid & 2u) {
           s.sb = __ldg(r.s + mstep + gi);
-          s.z |= (uint32_t)__ldg(r.z + mstep + gi) << 8;
+          s.zb = (uint32_t)__ldg(r.z + mstep + gi);
         }
       } else if constexpr (F == Fmt::MXFP4) {
         const int bi = kp >> 5;
-        s.z = 0x10000u;
-        if (r.valid & 1u) s.z |= (uint32_t)__ldg(r.z + bi);
-        if (r.valid & 2u) s.z |= (uint32_t)__ldg(r.z + mstep + bi) << 8;
+        s.sa = 1.0f;
+        if (r.valid & 1u) s.za = (uint32_t)__ldg(r.z + bi);
+        if (r.valid & 2u) s.zb = (uint32_t)__ldg(r.z + mstep + bi);
       } else {
         if (r.valid & 1u) s.sa = __ldg(r.s);
         if (r.valid & 2u) s.sb = __ldg(r.s + 8);
@@ -238,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM) k_gemv(const GemvParam
     } else {
       s.a = s.b = make_uint4(0, 0, 0, 0);
       s.sa = s.sb = 0.0f;
-      s.z = 0u;
+      s.za = s.zb = 0u;
     }
     ++pg;
     if (++pch == cpt) {
@@ -330,15 +402,15 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM) k_gemv(const GemvParam
           Nib8Consts kA, kB;
           float2 XA, XB;
           if constexpr (F == Fmt::I4G) {
-            kA = make_nib8_consts_u(s.sa, s.z & 0xFFu);
-            kB = make_nib8_consts_u(s.sb, (s.z >> 8) & 0xFFu);
+            kA = make_nib8_consts_u(s.sa, s.za);
+            kB = make_nib8_consts_u(s.sb, s.zb);
           } else if constexpr (F == Fmt::I4R) {
             kA = make_nib8_consts(s.sa, 8.0f);
             kB = make_nib8_consts(s.sb, 8.0f);
           } else {
-            const bool ok = (s.z >> 16) != 0u;
-            const float xa = ok ? e8m0_to_f32(s.z & 0xFFu) : 0.0f;
-            const float xb = ok ? e8m0_to_f32((s.z >> 8) & 0xFFu) : 0.0f;
+            const bool ok = s.sa != 0.0f;
+            const float xa = ok ? e8m0_to_f32(s.za) : 0.0f;
+            const float xb = ok ? e8m0_to_f32(s.zb) : 0.0f;
             XA = make_float2(xa, xa);
             XB = make_float2(xb, xb);
           }
@@ -444,70 +516,334 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM) k_gemv(const GemvParam
     }
   }
 
-  // ---- finish the tiles cut by a warp boundary (stream-K only) ----
-  // Each contributing warp adds one to the tile's counter once its partial is out; the
-  // one that brings it to the number of contributors adds the partials in warp order,
-  // writes y and clears the counter.  Nobody waits on anybody.
-  const int64_t W = items * cpt;
-  // range boundary c * W / G of warp c: 32-bit arithmetic when the product fits
-  const bool narrow = (uint64_t)W * (uint64_t)G < (1ull << 32);
-  auto bound = [&](int64_t cc) -> int64_t {
-    return narrow ? (int64_t)((uint32_t)cc * (uint32_t)W / (uint32_t)G) : cc * W / G;
-  };
-  auto owner = [&](int64_t sidx) -> int64_t {
-    int64_t cc = narrow ? (int64_t)((uint32_t)sidx * (uint32_t)G / (uint32_t)W) : sidx * G / W;
-    while (cc + 1 < G && bound(cc + 1) <= sidx) ++cc;
-    while (cc > 0 && bound(cc) > sidx) --cc;
-    return cc;
-  };
-  for (int i = 0; i < npend; ++i) {
-    const int tile = pend_tile[i];
-    // the lanes' partial stores happen before lane 0's fence (warp barrier), and the
-    // fence before its arrival on the counter
-    __syncwarp();
-    if (lane == 0) __threadfence();
-    const int64_t t_beg = (int64_t)tile * cpt;
-    const int64_t c0 = owner(t_beg), c1 = owner(t_beg + cpt - 1);
-    // warps between c0 and c1 whose range is empty (fewer chunks than warps) take no part
-    uint32_t contributors = 0;
-    for (int64_t cc = c0; cc <= c1; ++cc)
-      if (bound(cc) < bound(cc + 1)) ++contributors;
-    int last = 0;
-    if (lane == 0) last = (atomicAdd(&p.ws_cnt[tile], 1u) == contributors - 1u) ? 1 : 0;
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (last) {
-      __threadfence();
-      for (int idx = lane; idx < p.M * kRows; idx += 32) {
-        const int m = idx / kRows, row = idx % kRows;
-        // independent loads four at a time, added in warp order
-        float v = 0.0f;
-        for (int64_t cc0 = c0; cc0 <= c1; cc0 += 4) {
-          float part[4];
+  finish_cut_tiles(p, c, G, items * cpt, cpt, pend_tile, npend, lane);
+}
+
+// ------------------------------------------------------------------ factored decode
+// Formats I4G with a group of at least 128 codes, I4R and I8R; any number of activation
+// rows (batches of 8 * MT).
+//
+// Within one 64-byte chunk of a row (128 4-bit codes, or 64 int8 codes) the scale s and
+// the zero point z are constant, so the chunk's share of the dot product is
+//     sum_k x[k] * ((q[k] - z) * s)  =  s * sum_k x[k] * (q[k] - z):
+// the per-element product of the definition, reassociated ("Quantization" (Linnet docs):
+// dequantize_int4_groups forms (q - zero) * scale per element in f32 and casts it to
+// bf16; here that product is not rounded to bf16 and s is applied once a chunk).  q - z
+// is a small integer and is formed exactly in bf16x2:
+//   * 4-bit: the nibble q in the low mantissa bits of the bf16 128.0 (one logic op) is
+//     128 + q; subtracting the bf16 128 + z (exact for z <= 127) leaves q - z.  Larger
+//     zero points take a second exact subtraction (a warp-uniform slow path);
+//   * int8: the byte q + 128 in the mantissa of the f32 2^23, minus 2^23 + 128, is q,
+//     exact in bf16 since |q| <= 128.
+// The chunk's sum then runs on the warp MMA (m16n8k16, bf16 in, f32 accumulate): the
+// products x * (q - z) are exact and only the f32 sums round, as in any f32 dot product.
+// A word of eight 4-bit codes costs seven logic/shift ops, four packed subtractions and
+// a quarter of an MMA a lane, against an f32 multiply and a conversion to bf16 for
+// every element when the weights are dequantized first.
+//
+// Lane layout, work split and stream-K fixup are those of k_gemv.  The k order inside an
+// MMA is a permutation shared by A and B: the nibble extraction yields the pairs
+// (k, k + 4) of a word, so each lane permutes its activations into the same pairs once a
+// chunk (shared by both rows and every MMA of the chunk).
+namespace {
+
+// Four int8 codes of a word as exact bf16x2 pairs (k0, k1) and (k2, k3).
+__device__ __forceinline__ void i8x4_to_bf16x2(uint32_t w, uint32_t (&out)[2]) {
+  const uint32_t u = w ^ 0x80808080u;                      // bytes q + 128
+  const float2 c = make_float2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
+  const float2 f01 =
+      __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440)),
+                             __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441))), c);
+  const float2 f23 =
+      __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7442)),
+                             __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443))), c);
+  out[0] = pack_bf16x2(f01.x, f01.y);
+  out[1] = pack_bf16x2(f23.x, f23.y);
+}
+
+// Eight 4-bit codes of a word (even element in the low nibble) minus a zero point, as
+// exact bf16x2 pairs d[j] = (k j, k j + 4).  zc = bf16x2 of 128 + min(z, 127); zc2 = bf16x2
+// of max(z - 127, 0), used only when `big`.
+template <bool kBig>
+__device__ __forceinline__ void nib8_minus_zero(uint32_t w, uint32_t zc, uint32_t zc2,
+                                                uint32_t (&d)[4]) {
+  d[0] = sub_bf16x2((w & 0x000F000Fu) | 0x43004300u, zc);
+  d[1] = sub_bf16x2(((w >> 4) & 0x000F000Fu) | 0x43004300u, zc);
+  d[2] = sub_bf16x2(((w >> 8) & 0x000F000Fu) | 0x43004300u, zc);
+  d[3] = sub_bf16x2(((w >> 12) & 0x000F000Fu) | 0x43004300u, zc);
+  if constexpr (kBig) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int64_t cc = cc0 + q;
-            part[q] = 0.0f;
-            if (cc <= c1) {
-              const int64_t b0 = bound(cc);
-              if (b0 != bound(cc + 1)) {
-                const int sid = (b0 >= t_beg) ? 0 : 1;
-                part[q] = __ldcg(&p.ws_part[((cc * 2 + sid) * p.M + m) * kRows + row]);
+    for (int j = 0; j < 4; ++j) d[j] = sub_bf16x2(d[j], zc2);
+  }
+}
+
+}  // namespace
+
+// A warp streams its range of (tile, step) units; a step is two chunks, i.e. 128
+// contiguous bytes of each of the tile's 16 rows, so that consecutive requests of a warp
+// cover whole DRAM bursts.  The hot loop carries no per-lane predicate: row indices past
+// N are clamped to the last row (those outputs are never stored) and activation rows
+// past M to the last one (those MMA columns are never stored); only a warp-uniform test
+// stops the prefetch at the end of the range.  Rows must hold a whole number of steps
+// (checked by the host).
+template <Fmt F, int MT>
+__global__ void __launch_bounds__(kThreads, kBlocksPerSM) k_gemv_fact(const GemvParams p) {
+  static_assert(F == Fmt::I4G || F == Fmt::I4R || F == Fmt::I8R, "affine formats only");
+  constexpr int kPiece = piece_k<F>();   // k of a lane's 16 bytes
+  constexpr int kChunkK = chunk_k<F>();  // k of a 64-byte chunk
+  constexpr int kXR = kPiece / 2;        // bf16x2 registers of x a piece
+  constexpr int kBatch = 8 * MT;         // activation rows an item
+  constexpr int kStepBytes = 2 * kChunkBytes;
+  constexpr int kD = 1;                  // steps in flight a warp (two chunks)
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g8 = lane >> 2;  // MMA row group: tile rows g8 and g8 + 8
+  const int cq = lane & 3;   // 16-byte piece of a chunk
+  const int64_t N = p.N;
+  const int64_t K = p.K;
+  const int64_t M = p.M;
+  const int tiles = (int)((N + kRows - 1) / kRows);
+  const int64_t row_bytes = (F == Fmt::I8R) ? K : K / 2;
+  const int spt = (int)(row_bytes / kStepBytes);  // steps a tile
+  const int64_t items = (int64_t)tiles * ((M + kBatch - 1) / kBatch);
+  const bool stream_k = (p.ws_cnt != nullptr);     // partial tiles allowed (one batch only)
+  const int64_t G = (int64_t)gridDim.x * kWarps;
+  const int64_t c = (int64_t)blockIdx.x * kWarps + warp;
+  const int64_t beg = warp_begin(c, G, items, spt, !stream_k);
+  const int64_t end = warp_begin(c + 1, G, items, spt, !stream_k);
+  if (beg >= end) return;  // no block-wide synchronization after this point
+  const int gshift = p.group_shift;
+  const int64_t gpr = (F == Fmt::I4G) ? (K >> gshift) : 0;  // scales a row (I4G)
+
+  // ---- prefetch cursor, kD steps ahead of the main one ----
+  struct Step {
+    uint4 a0, a1, b0, b1;  // chunks 0 and 1 of rows A (tile row g8) and B (g8 + 8)
+    float sa0, sa1, sb0, sb1;
+    uint32_t za0, za1, zb0, zb1;  // I4G zero points, each in a register of its own
+  };
+  int64_t pu = beg;
+  int64_t pitem = beg / spt;
+  int pst = (int)(beg % spt);
+  const uint8_t* pwA = nullptr;
+  const uint8_t* pwB = nullptr;
+  const float* psA = nullptr;
+  const float* psB = nullptr;
+  const uint8_t* pzA = nullptr;
+  const uint8_t* pzB = nullptr;
+  auto set_prow = [&](int64_t item) {
+    const int64_t t0 = (item % tiles) * kRows;
+    const int64_t rA = imin64(t0 + g8, N - 1), rB = imin64(t0 + g8 + 8, N - 1);
+    pwA = p.w + rA * row_bytes + cq * 16;
+    pwB = p.w + rB * row_bytes + cq * 16;
+    if constexpr (F == Fmt::I4G) {
+      psA = p.scale + rA * gpr;
+      psB = p.scale + rB * gpr;
+      pzA = p.zero + rA * gpr;
+      pzB = p.zero + rB * gpr;
+    } else {
+      psA = p.scale + rA;
+      psB = p.scale + rB;
+    }
+  };
+  set_prow(pitem);
+  auto fetch = [&](Step& s) {
+    if (pu < end) {  // warp-uniform
+      const uint32_t off = (uint32_t)pst * kStepBytes;
+      s.a0 = ld_global_stream_v4(pwA + off);
+      s.a1 = ld_global_stream_v4(pwA + off + kChunkBytes);
+      s.b0 = ld_global_stream_v4(pwB + off);
+      s.b1 = ld_global_stream_v4(pwB + off + kChunkBytes);
+      if constexpr (F == Fmt::I4G) {
+        const int g0 = (pst * 2 * kChunkK) >> gshift, g1 = ((pst * 2 + 1) * kChunkK) >> gshift;
+        s.sa0 = __ldg(psA + g0);
+        s.sa1 = __ldg(psA + g1);
+        s.sb0 = __ldg(psB + g0);
+        s.sb1 = __ldg(psB + g1);
+        s.za0 = __ldg(pzA + g0);
+        s.za1 = __ldg(pzA + g1);
+        s.zb0 = __ldg(pzB + g0);
+        s.zb1 = __ldg(pzB + g1);
+      } else {
+        s.sa0 = s.sa1 = __ldg(psA);
+        s.sb0 = s.sb1 = __ldg(psB);
+      }
+      ++pu;
+      if (++pst == spt) {
+        pst = 0;
+        ++pitem;
+        if (pu < end) set_prow(pitem);
+      }
+    }
+  };
+  Step ring[kD];
+#pragma unroll
+  for (int j = 0; j < kD; ++j) fetch(ring[j]);
+
+  // ---- main cursor ----
+  int64_t item = beg / spt;
+  int st = (int)(beg % spt);
+  const __nv_bfloat16* xrow[MT];  // activation row tt * 8 + g8 of the item's batch (clamped)
+  auto set_xrow = [&]() {
+    const int64_t b0 = (item / tiles) * kBatch;
+#pragma unroll
+    for (int tt = 0; tt < MT; ++tt) xrow[tt] = p.x + imin64(b0 + tt * 8 + g8, M - 1) * K + cq * kPiece;
+  };
+  set_xrow();
+  float tot[MT][4];  // D fragments of the segment, scaled: rows g8 / g8 + 8, columns 2cq, 2cq+1
+#pragma unroll
+  for (int tt = 0; tt < MT; ++tt) tot[tt][0] = tot[tt][1] = tot[tt][2] = tot[tt][3] = 0.0f;
+  bool seg_first = true;             // the segment holds this warp's first step
+  bool seg_from_start = (st == 0);   // the segment began at step 0 of its tile
+  int pend_tile[2] = {-1, -1};       // tiles cut by this warp's range boundaries
+  int npend = 0;
+
+  // one chunk: tot += s (.) (W-chunk - z) x-chunk on the MMA
+  auto chunk = [&](const uint4& wa, const uint4& wb, float sa, float sb, uint32_t za, uint32_t zb,
+                   int kx) {
+    uint32_t xr[MT][kXR];
+#pragma unroll
+    for (int tt = 0; tt < MT; ++tt) {
+#pragma unroll
+      for (int q = 0; q < kXR / 4; ++q) {
+        const uint4 v = ld_global_nc_v4(xrow[tt] + kx + q * 8);
+        if constexpr (F == Fmt::I8R) {
+          xr[tt][4 * q + 0] = v.x;
+          xr[tt][4 * q + 1] = v.y;
+          xr[tt][4 * q + 2] = v.z;
+          xr[tt][4 * q + 3] = v.w;
+        } else {
+          // word q of the piece holds elements 8q..8q+7: pairs (8q + j, 8q + j + 4)
+          xr[tt][4 * q + 0] = __byte_perm(v.x, v.z, 0x5410);
+          xr[tt][4 * q + 1] = __byte_perm(v.x, v.z, 0x7632);
+          xr[tt][4 * q + 2] = __byte_perm(v.y, v.w, 0x5410);
+          xr[tt][4 * q + 3] = __byte_perm(v.y, v.w, 0x7632);
+        }
+      }
+    }
+    float acc[MT][2][4];
+#pragma unroll
+    for (int tt = 0; tt < MT; ++tt)
+#pragma unroll
+      for (int a = 0; a < 2; ++a) acc[tt][a][0] = acc[tt][a][1] = acc[tt][a][2] = acc[tt][a][3] = 0.0f;
+    const uint32_t wA[4] = {wa.x, wa.y, wa.z, wa.w};
+    const uint32_t wB[4] = {wb.x, wb.y, wb.z, wb.w};
+    if constexpr (F == Fmt::I8R) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint32_t ga[2], gb[2];
+        i8x4_to_bf16x2(wA[i], ga);
+        i8x4_to_bf16x2(wB[i], gb);
+#pragma unroll
+        for (int tt = 0; tt < MT; ++tt)
+          mma_bf16_16816(acc[tt][i & 1], ga[0], gb[0], ga[1], gb[1], xr[tt][2 * i],
+                         xr[tt][2 * i + 1]);
+      }
+    } else {
+      auto mac = [&](auto big_tag, uint32_t zcA, uint32_t zcB, uint32_t zc2A, uint32_t zc2B) {
+        constexpr bool kBig = decltype(big_tag)::value;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint32_t da[4], db[4];
+          const uint32_t a = (F == Fmt::I4R) ? (wA[i] ^ 0x88888888u) : wA[i];
+          const uint32_t b = (F == Fmt::I4R) ? (wB[i] ^ 0x88888888u) : wB[i];
+          nib8_minus_zero<kBig>(a, zcA, zc2A, da);
+          nib8_minus_zero<kBig>(b, zcB, zc2B, db);
+#pragma unroll
+          for (int tt = 0; tt < MT; ++tt) {
+            mma_bf16_16816(acc[tt][0], da[0], db[0], da[1], db[1], xr[tt][4 * i],
+                           xr[tt][4 * i + 1]);
+            mma_bf16_16816(acc[tt][1], da[2], db[2], da[3], db[3], xr[tt][4 * i + 2],
+                           xr[tt][4 * i + 3]);
+          }
+        }
+      };
+      if constexpr (F == Fmt::I4R) {
+        // signed nibble v: (v ^ 8) = v + 8 in 0..15, zero point 8 (bf16 136)
+        mac(std::false_type{}, 0x43084308u, 0x43084308u, 0u, 0u);
+      } else if (__all_sync(0xffffffffu, ((za | zb) & 0x80u) == 0u)) {
+        mac(std::false_type{}, 0x43004300u | (za * 0x00010001u), 0x43004300u | (zb * 0x00010001u),
+            0u, 0u);
+      } else {
+        // zero points above 127: subtract 128 + min(z, 127), then max(z - 127, 0)
+        const uint32_t zA1 = min(za, 127u), zB1 = min(zb, 127u);
+        const uint32_t hA = __bfloat16_as_ushort(__float2bfloat16_rn((float)(za - zA1)));
+        const uint32_t hB = __bfloat16_as_ushort(__float2bfloat16_rn((float)(zb - zB1)));
+        mac(std::true_type{}, 0x43004300u | (zA1 * 0x00010001u), 0x43004300u | (zB1 * 0x00010001u),
+            hA * 0x00010001u, hB * 0x00010001u);
+      }
+    }
+#pragma unroll
+    for (int tt = 0; tt < MT; ++tt) {
+      tot[tt][0] = fmaf(sa, acc[tt][0][0] + acc[tt][1][0], tot[tt][0]);
+      tot[tt][1] = fmaf(sa, acc[tt][0][1] + acc[tt][1][1], tot[tt][1]);
+      tot[tt][2] = fmaf(sb, acc[tt][0][2] + acc[tt][1][2], tot[tt][2]);
+      tot[tt][3] = fmaf(sb, acc[tt][0][3] + acc[tt][1][3], tot[tt][3]);
+    }
+  };
+
+  const int total = (int)(end - beg);
+  for (int u0 = 0; u0 < total; u0 += kD) {
+#pragma unroll
+    for (int j = 0; j < kD; ++j) {
+      if (u0 + j < total) {
+        const Step s = ring[j];
+        fetch(ring[j]);
+        const int kx = st * 2 * kChunkK;
+        chunk(s.a0, s.b0, s.sa0, s.sb0, s.za0, s.zb0, kx);
+        chunk(s.a1, s.b1, s.sa1, s.sb1, s.za1, s.zb1, kx + kChunkK);
+
+        // ---- end of a segment: the tile ends here, or this warp's range does ----
+        const bool tile_end = (st == spt - 1);
+        if (tile_end || u0 + j + 1 == total) {
+          const bool full_tile = seg_from_start && tile_end;
+          const int tile = (int)(item % tiles);
+          const int slot_id = seg_first ? 0 : 1;
+          const int64_t b0 = (item / tiles) * kBatch;
+#pragma unroll
+          for (int tt = 0; tt < MT; ++tt) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              // D fragment: i = 0, 1 -> row g8, columns 2cq, 2cq+1; i = 2, 3 -> row g8 + 8
+              const float v = tot[tt][i];
+              tot[tt][i] = 0.0f;
+              const int64_t m = b0 + tt * 8 + 2 * cq + (i & 1);
+              const int row = g8 + ((i >> 1) << 3);
+              const int64_t n = (int64_t)tile * kRows + row;
+              if (m < M) {
+                if (full_tile) {
+                  if (n < N) {
+                    const float bias = p.bias ? __bfloat162float(p.bias[n]) : 0.0f;
+                    p.y[m * N + n] = __float2bfloat16_rn(v + bias);
+                  }
+                } else {
+                  p.ws_part[((c * 2 + slot_id) * M + m) * kRows + row] = v;
+                }
               }
             }
           }
-#pragma unroll
-          for (int q = 0; q < 4; ++q) v += part[q];
+          if (!full_tile) pend_tile[npend++] = tile;
+          seg_first = false;
+          seg_from_start = true;
         }
-        const int64_t n = (int64_t)tile * kRows + row;
-        if (n < N) {
-          if (p.bias) v += __bfloat162float(p.bias[n]);
-          p.y[(int64_t)m * N + n] = __float2bfloat16_rn(v);
+
+        // ---- advance the main cursor ----
+        if (++st == spt) {
+          st = 0;
+          ++item;
+          if (u0 + j + 1 < total) set_xrow();
         }
       }
-      __syncwarp();
-      if (lane == 0) p.ws_cnt[tile] = 0u;
     }
   }
+
+  finish_cut_tiles(p, c, G, items * spt, spt, pend_tile, npend, lane);
+}
+
+// Rows of the factored kernel hold whole steps (two 64-byte chunks).
+bool fact_shape_ok(Fmt f, int64_t K) {
+  const int64_t row_bytes = (f == Fmt::I8R) ? K : K / 2;
+  return row_bytes % (2 * kChunkBytes) == 0;
 }
 
 // ------------------------------------------------------------------ host side
@@ -520,10 +856,21 @@ cudaError_t launch_t(const GemvParams& p, int grid, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-// One or two activation rows: FMA pipe; more: warp MMA in groups of 8 (16 at most a
-// batch, larger M loops over batches).
+template <Fmt F, int MT>
+cudaError_t launch_fact(const GemvParams& p, int grid, cudaStream_t stream) {
+  k_gemv_fact<F, MT><<<grid, kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+// I4G with a group of at least 128 codes, I4R, I8R: the factored kernel (warp MMA,
+// batches of 8 or 16 activation rows).  I4G with smaller groups and MXFP4: the exact
+// kernel, on the FMA pipe for one or two rows and on the warp MMA for more.
 template <Fmt F>
 cudaError_t launch_f(const GemvParams& p, int64_t rows, int grid, cudaStream_t stream) {
+  if constexpr (F != Fmt::MXFP4) {
+    if ((F != Fmt::I4G || p.group >= 128) && fact_shape_ok(F, p.K))
+      return rows <= 8 ? launch_fact<F, 1>(p, grid, stream) : launch_fact<F, 2>(p, grid, stream);
+  }
   if (rows <= 1) return launch_t<F, 1, true>(p, grid, stream);
   if (rows <= 2) return launch_t<F, 2, true>(p, grid, stream);
   if (rows <= 8) return launch_t<F, 1, false>(p, grid, stream);
