@@ -74,6 +74,9 @@ CASES = [
     (9, 64, 1024, 32, False),
     (16, 1024, 4096, 128, True),
     (17, 100, 512, 128, False),           # multiple activation batches
+    (1, 1000, 2048, 128, True),           # factored kernel: ragged N, TMA boxes past N
+    (3, 48, 4096, 256, False),
+    (24, 200, 4096, 128, True),           # factored kernel, two batches of 16
     (40, 48, 1024, 64, True),             # tensor-core regime from here on
     (32, 256, 256, 32, False),
     (256, 512, 4096, 128, True),
@@ -94,6 +97,23 @@ def test_int4_groups_shapes(cuda_device, M, N, K, G, bias, use_ws):
     yr, ad = oracle.linear_int4_groups(bf16_bits(x), packed, scale, zero, None if b is None else bf16_bits(b),
                                        N, G)
     assert_within(y, yr, ad, f"M={M} N={N} K={K} G={G}")
+
+
+@pytest.mark.parametrize("M,G", [(1, 128), (5, 128), (1, 256), (13, 64), (2, 32)])
+def test_int4_groups_zero_points_over_full_byte_range(cuda_device, M, G):
+    """The layout stores zero points as u8: codes minus any zero point 0..255 (above 127
+    the factored kernel takes its two-subtraction path) match the oracle."""
+    d = cuda_device
+    N, K = 200, 2048
+    rng = np.random.default_rng(M * 7 + G)
+    packed = rng.integers(0, 256, (N, K // 2)).astype(np.uint8)
+    scale = (rng.random((N, K // G)) * 0.018 + 0.002).astype(np.float32)
+    zero = rng.integers(0, 256, (N, K // G)).astype(np.uint8)
+    zero[:8] = 255           # whole tiles of large zero points, and mixed warps elsewhere
+    x = synth.normal_bf16((M, K), seed=M + 11)
+    y = run_i4g(d, dev(x, d), dev(packed, d), dev(scale, d), dev(zero, d), None, G)
+    yr, ad = oracle.linear_int4_groups(bf16_bits(x), packed, scale, zero, None, N, G)
+    assert_within(y, yr, ad, f"full-range zero points M={M} G={G}")
 
 
 def test_int4_groups_deterministic_and_split_invariant(cuda_device, monkeypatch):
@@ -249,10 +269,12 @@ def test_mxfp4_many_rows_per_expert_and_bad_index(cuda_device):
 @pytest.mark.parametrize("grid", [1, 3, 7, 64, 151])
 @pytest.mark.parametrize("M", [1, 13])
 def test_stream_k_partitions(cuda_device, monkeypatch, grid, M):
-    """Every block count gives the same answer: tiles cut anywhere by the equal-share
-    ranges are finished from their partials (deterministically)."""
+    """Every block (exact kernel) or cluster (factored kernel) count gives the same
+    answer: tiles cut anywhere by the equal-share ranges are finished from their partials
+    (deterministically)."""
     d = cuda_device
     monkeypatch.setenv("WQ_GEMV_BLOCKS", str(grid))
+    monkeypatch.setenv("WQ_GEMV_CLUSTERS", str(grid))
     N, K, G = 1000, 4096 + 1024, 128
     packed, scale, zero = make_i4g(N, K, G, seed=grid)
     x = synth.normal_bf16((M, K), seed=grid + 1)

@@ -75,6 +75,61 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// ------------------------------------------------------------------ thread-block clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_count_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster arrives (release) and waits (acquire): shared
+// memory written before it is visible to the cluster's CTAs after it.  A hardware
+// barrier: all threads must reach it (no early exit before it).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The shared::cluster address of a shared::cta address in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_shared_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float4 ld_shared_cluster_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// ------------------------------------------------------------------ programmatic dependent launch
+// Allow the next kernel of the stream (launched with programmatic stream serialization)
+// to be scheduled now; it still waits for this grid's completion in grid_dep_wait().
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the grids this one depends on have completed and their memory is visible.
+// Nothing written by an earlier kernel may be read, and nothing an earlier kernel reads
+// may be written, before this.
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ TMA (bulk tensor)
 // 2-D tile load global -> shared, completing `bytes` on the mbarrier.  Coordinates are
 // in elements of the tensor map (innermost first).  `policy` is an L2 cache policy.
@@ -109,11 +164,22 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
                : "r"(addr));
   return v;
 }
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_shared_u8(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
 // Read-only 16-byte global load that stays in L1 (activations are reused by every
-// thread block of the SM).
+// thread block of the SM).  Not volatile: the data never changes during a kernel, so the
+// compiler may hoist and interleave these loads freely.
 __device__ __forceinline__ uint4 ld_global_nc_v4(const void* p) {
   uint4 v;
-  asm volatile("ld.global.nc.v4.b32 {%0, %1, %2, %3}, [%4];"
+  asm("ld.global.nc.v4.b32 {%0, %1, %2, %3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
   return v;
@@ -134,11 +200,12 @@ __device__ __forceinline__ uint4 ld_global_stream_v4(const void* p) {
 }
 
 // ------------------------------------------------------------------ warp MMA
-// D(16x8, f32) += A(16x16, bf16, row-major) * B(16x8, bf16, column-major).
+// D(16x8, f32) += A(16x16, bf16, row-major) * B(16x8, bf16, column-major).  A pure
+// function of its operands (not volatile), so that the compiler can overlap it with loads.
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
                                                uint32_t a2, uint32_t a3, uint32_t b0,
                                                uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
       "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -170,6 +237,14 @@ __device__ __forceinline__ void fma_mix(float& acc, uint32_t a, uint32_t b) {
   else
     asm("{\n .reg .b16 a0, a1, b0, b1;\n mov.b32 {a0, a1}, %1;\n mov.b32 {b0, b1}, %2;\n"
         " fma.rn.f32.bf16 %0, a1, b1, %0;\n}" : "+f"(acc) : "r"(a), "r"(b));
+}
+
+// (a & 0x000F000F) | c as one logic op.  c is passed in a register: with two immediate
+// constants the compiler splits the expression into two logic ops.
+__device__ __forceinline__ uint32_t and_0f_or(uint32_t a, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, 0x000F000F, %2, 0xEA;" : "=r"(d) : "r"(a), "r"(c));
+  return d;
 }
 
 // Packed bf16 subtraction a - b, rounded to nearest even (exact for the small integers

@@ -563,14 +563,17 @@ __device__ __forceinline__ void i8x4_to_bf16x2(uint32_t w, uint32_t (&out)[2]) {
 
 // Eight 4-bit codes of a word (even element in the low nibble) minus a zero point, as
 // exact bf16x2 pairs d[j] = (k j, k j + 4).  zc = bf16x2 of 128 + min(z, 127); zc2 = bf16x2
-// of max(z - 127, 0), used only when `big`.
+// of max(z - 127, 0), used only when `big`; magic = 0x43004300 (bf16x2 128, 128) held in a
+// register.
 template <bool kBig>
 __device__ __forceinline__ void nib8_minus_zero(uint32_t w, uint32_t zc, uint32_t zc2,
-                                                uint32_t (&d)[4]) {
-  d[0] = sub_bf16x2((w & 0x000F000Fu) | 0x43004300u, zc);
-  d[1] = sub_bf16x2(((w >> 4) & 0x000F000Fu) | 0x43004300u, zc);
-  d[2] = sub_bf16x2(((w >> 8) & 0x000F000Fu) | 0x43004300u, zc);
-  d[3] = sub_bf16x2(((w >> 12) & 0x000F000Fu) | 0x43004300u, zc);
+                                                uint32_t magic, uint32_t (&d)[4]) {
+  // the shifts as high halves of products (w >> s = hi32(w * 2^(32 - s))): they run on
+  // the FMA pipe, leaving the logic pipe to the masks
+  d[0] = sub_bf16x2(and_0f_or(w, magic), zc);
+  d[1] = sub_bf16x2(and_0f_or(__umulhi(w, 1u << 28), magic), zc);
+  d[2] = sub_bf16x2(and_0f_or(__umulhi(w, 1u << 24), magic), zc);
+  d[3] = sub_bf16x2(and_0f_or(__umulhi(w, 1u << 20), magic), zc);
   if constexpr (kBig) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) d[j] = sub_bf16x2(d[j], zc2);
@@ -579,113 +582,179 @@ __device__ __forceinline__ void nib8_minus_zero(uint32_t w, uint32_t zc, uint32_
 
 }  // namespace
 
-// A warp streams its range of (tile, step) units; a step is two chunks, i.e. 128
-// contiguous bytes of each of the tile's 16 rows, so that consecutive requests of a warp
-// cover whole DRAM bursts.  The hot loop carries no per-lane predicate: row indices past
-// N are clamped to the last row (those outputs are never stored) and activation rows
-// past M to the last one (those MMA columns are never stored); only a warp-uniform test
-// stops the prefetch at the end of the range.  Rows must hold a whole number of steps
-// (checked by the host).
+namespace {
+
+// The factored kernel runs in clusters of kFactCluster CTAs (kFactWarps warps).
+constexpr int kFactCluster = 8;
+constexpr int kFactWarps = kFactCluster * kWarps;
+constexpr int kFactWarpsLog2 = 6;
+static_assert((1 << kFactWarpsLog2) == kFactWarps, "warps a cluster: a power of two");
+
+// Write a finished tile's D fragments (rows g8 / g8 + 8, columns 2cq, 2cq + 1 of each
+// group of 8 activation rows) to y, adding the bias.
+template <int MT>
+__device__ __forceinline__ void emit_tile(const GemvParams& p, int64_t item, int tiles, int batch,
+                                          const float (&tot)[MT][4], int g8, int cq) {
+  const int64_t tile = item % tiles;
+  const int64_t b0 = (item / tiles) * batch;
+#pragma unroll
+  for (int tt = 0; tt < MT; ++tt) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t m = b0 + tt * 8 + 2 * cq + (i & 1);
+      const int64_t n = tile * kRows + g8 + ((i >> 1) << 3);
+      if (m < p.M && n < p.N) {
+        const float bias = p.bias ? __bfloat162float(p.bias[n]) : 0.0f;
+        p.y[m * p.N + n] = __float2bfloat16_rn(tot[tt][i] + bias);
+      }
+    }
+  }
+}
+
+}  // namespace
+
+// Work split: launched in clusters of CTAs (thread-block clusters).  Each cluster takes
+// a contiguous range of whole items (a 16-row tile and a batch of activation rows); the
+// cluster's warps split its (item, step) units evenly, a step being two chunks, i.e. 128
+// contiguous bytes of each of the tile's 16 rows.  A tile whose units fall to one warp is
+// written to y by that warp; a tile cut between warps is finished inside the cluster:
+// each contributor leaves its partial D fragment in its own shared-memory slot, and
+// after a cluster barrier the warp that holds the tile's last step adds the
+// contributors' slots in warp order (deterministic), reading the other CTAs' slots
+// through distributed shared memory.  No workspace, atomics or memory fences.
+//
+// Loads: every warp streams its steps through its own ring of kFactStages shared-memory
+// stages filled by TMA (a {128 bytes, 16 rows} box of codes with the 128-byte swizzle,
+// and the step's scales and zero points), one mbarrier a stage; kFactStages - 1 steps
+// are in flight while one is computed, independent of the register budget.  Rows past N
+// arrive as zeros (TMA fills out-of-bounds boxes) and are never stored.  Activation rows
+// past M are clamped to the last one (those MMA columns are never stored).
+struct FactMaps {
+  CUtensorMap w;  // codes [N rows, row_bytes], box {128, 16}, 128-byte swizzle
+  CUtensorMap s;  // I4G: scales [N, K/G] f32, box {4, 16}; I4R / I8R: scales [N] f32, box {16, 1}
+  CUtensorMap z;  // I4G: zero points [N, K/G] u8, box {16, 16}
+};
+
+constexpr int kFactStages = 4;
+constexpr int kFactStageW = 2048;  // code bytes a stage (16 rows x 128)
+constexpr int kFactStageS = 256;   // scale bytes a stage (I4G: 16 rows x 4 groups)
+constexpr int kFactStageZ = 256;   // zero-point bytes a stage (16 rows x 16 groups)
+// dynamic shared memory: codes (1024-byte aligned for the swizzle), scales, zero points,
+// barriers; plus slack for the alignment
+constexpr int kFactSmemBytes =
+    kWarps * kFactStages * (kFactStageW + kFactStageS + kFactStageZ + 8) + 1024;
+
 template <Fmt F, int MT>
-__global__ void __launch_bounds__(kThreads, kBlocksPerSM) k_gemv_fact(const GemvParams p) {
+__global__ void __launch_bounds__(kThreads, kBlocksPerSM)
+    k_gemv_fact(const GemvParams p, const __grid_constant__ FactMaps maps) {
   static_assert(F == Fmt::I4G || F == Fmt::I4R || F == Fmt::I8R, "affine formats only");
   constexpr int kPiece = piece_k<F>();   // k of a lane's 16 bytes
   constexpr int kChunkK = chunk_k<F>();  // k of a 64-byte chunk
   constexpr int kXR = kPiece / 2;        // bf16x2 registers of x a piece
   constexpr int kBatch = 8 * MT;         // activation rows an item
-  constexpr int kStepBytes = 2 * kChunkBytes;
-  constexpr int kD = 1;                  // steps in flight a warp (two chunks)
+  constexpr int kS = kFactStages;
+  constexpr uint32_t kStageTx =
+      kFactStageW + ((F == Fmt::I4G) ? kFactStageS + kFactStageZ : 16 * 4);
+  // partial D fragments of cut tiles: [warp][first / last segment][lane][4 * MT]
+  __shared__ __align__(16) float s_part[kWarps][2][32][4 * MT];
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
 
+  // the next kernel of the stream may be scheduled as our CTAs retire; its own
+  // grid_dep_wait() orders it after this grid
+  grid_dep_launch_dependents();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int g8 = lane >> 2;  // MMA row group: tile rows g8 and g8 + 8
   const int cq = lane & 3;   // 16-byte piece of a chunk
-  const int64_t N = p.N;
   const int64_t K = p.K;
   const int64_t M = p.M;
-  const int tiles = (int)((N + kRows - 1) / kRows);
+  const uint32_t tiles = (uint32_t)((p.N + kRows - 1) / kRows);
   const int64_t row_bytes = (F == Fmt::I8R) ? K : K / 2;
-  const int spt = (int)(row_bytes / kStepBytes);  // steps a tile
-  const int64_t items = (int64_t)tiles * ((M + kBatch - 1) / kBatch);
-  const bool stream_k = (p.ws_cnt != nullptr);     // partial tiles allowed (one batch only)
-  const int64_t G = (int64_t)gridDim.x * kWarps;
-  const int64_t c = (int64_t)blockIdx.x * kWarps + warp;
-  const int64_t beg = warp_begin(c, G, items, spt, !stream_k);
-  const int64_t end = warp_begin(c + 1, G, items, spt, !stream_k);
-  if (beg >= end) return;  // no block-wide synchronization after this point
+  const uint32_t spt = (uint32_t)(row_bytes / (2 * kChunkBytes));  // steps a tile
+  // items * spt < 2^31 (checked by the host): unit and item indices are 32-bit
+  const uint32_t items = tiles * (uint32_t)((M + kBatch - 1) / kBatch);
+
+  // this warp's ring
+  uint8_t* wst = smem + warp * kS * kFactStageW;
+  uint8_t* sst = smem + kWarps * kS * kFactStageW + warp * kS * kFactStageS;
+  uint8_t* zst = smem + kWarps * kS * (kFactStageW + kFactStageS) + warp * kS * kFactStageZ;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(
+      smem + kWarps * kS * (kFactStageW + kFactStageS + kFactStageZ) + warp * kS * 8);
+
+  // this cluster's items and units, and the first unit of warp w of the cluster (this
+  // warp is warp wc of kFactWarps); recomputed after the main loop rather than kept in
+  // registers.  Cluster c takes q or q + 1 items, q = items / clusters.
+  struct Split {
+    uint32_t u0, U, wc;
+    __device__ uint32_t bound(uint32_t w) const {
+      return u0 + (uint32_t)(((uint64_t)w * U) >> kFactWarpsLog2);
+    }
+  };
+  auto split = [&]() -> Split {
+    const uint32_t ncl = cluster_count_x(), cid = cluster_id_x();
+    const uint32_t q = items / ncl, r = items - q * ncl;
+    const uint32_t ibeg = cid * q + min(cid, r), icnt = q + (cid < r ? 1u : 0u);
+    return Split{ibeg * spt, icnt * spt, cluster_ctarank() * kWarps + warp};
+  };
+  uint32_t beg, end;
+  {
+    const Split sp = split();
+    beg = sp.bound(sp.wc);
+    end = sp.bound(sp.wc + 1);
+  }
   const int gshift = p.group_shift;
-  const int64_t gpr = (F == Fmt::I4G) ? (K >> gshift) : 0;  // scales a row (I4G)
+  // bf16x2 (128, 128), derived from a kernel argument so that it stays in a register
+  const uint32_t magic = 0x43004300u | (uint32_t)(p.K >> 62);
+  int close_item = -1;  // the cut tile this warp finishes after the cluster barrier
 
-  // ---- prefetch cursor, kD steps ahead of the main one ----
-  struct Step {
-    uint4 a0, a1, b0, b1;  // chunks 0 and 1 of rows A (tile row g8) and B (g8 + 8)
-    float sa0, sa1, sb0, sb1;
-    uint32_t za0, za1, zb0, zb1;  // I4G zero points, each in a register of its own
-  };
-  int64_t pu = beg;
-  int64_t pitem = beg / spt;
-  int pst = (int)(beg % spt);
-  const uint8_t* pwA = nullptr;
-  const uint8_t* pwB = nullptr;
-  const float* psA = nullptr;
-  const float* psB = nullptr;
-  const uint8_t* pzA = nullptr;
-  const uint8_t* pzB = nullptr;
-  auto set_prow = [&](int64_t item) {
-    const int64_t t0 = (item % tiles) * kRows;
-    const int64_t rA = imin64(t0 + g8, N - 1), rB = imin64(t0 + g8 + 8, N - 1);
-    pwA = p.w + rA * row_bytes + cq * 16;
-    pwB = p.w + rB * row_bytes + cq * 16;
+  if (beg < end) {
+  const int total = (int)(end - beg);
+  // ---- producer side: lane 0 fills stage (u mod kS) with the data of unit beg + u; its
+  // cursor (tile row, step) advances one unit an issue ----
+  const uint64_t pol_stream = l2_policy_evict_first();
+  const uint64_t pol_keep = l2_policy_evict_last();
+  uint32_t i_st = beg % spt;
+  uint32_t i_tile = (beg / spt) % tiles;
+  auto issue = [&](int u) {
+    const uint32_t st = i_st;
+    const int32_t row0 = (int32_t)(i_tile * kRows);
+    if (++i_st == spt) {
+      i_st = 0;
+      if (++i_tile == tiles) i_tile = 0;
+    }
+    const int stage = u % kS;
+    uint64_t* bar = bars + stage;
+    mbar_arrive_expect_tx(bar, kStageTx);
+    tma_load_2d(wst + stage * kFactStageW, &maps.w, bar, (int32_t)(st * 2 * kChunkBytes), row0,
+                pol_stream);
     if constexpr (F == Fmt::I4G) {
-      psA = p.scale + rA * gpr;
-      psB = p.scale + rB * gpr;
-      pzA = p.zero + rA * gpr;
-      pzB = p.zero + rB * gpr;
+      const int32_t g0 = (int32_t)((st * 2 * kChunkK) >> gshift);
+      tma_load_2d(sst + stage * kFactStageS, &maps.s, bar, g0 & ~3, row0, pol_keep);
+      tma_load_2d(zst + stage * kFactStageZ, &maps.z, bar, g0 & ~15, row0, pol_keep);
     } else {
-      psA = p.scale + rA;
-      psB = p.scale + rB;
+      tma_load_2d(sst + stage * kFactStageS, &maps.s, bar, row0, 0, pol_keep);
     }
   };
-  set_prow(pitem);
-  auto fetch = [&](Step& s) {
-    if (pu < end) {  // warp-uniform
-      const uint32_t off = (uint32_t)pst * kStepBytes;
-      s.a0 = ld_global_stream_v4(pwA + off);
-      s.a1 = ld_global_stream_v4(pwA + off + kChunkBytes);
-      s.b0 = ld_global_stream_v4(pwB + off);
-      s.b1 = ld_global_stream_v4(pwB + off + kChunkBytes);
-      if constexpr (F == Fmt::I4G) {
-        const int g0 = (pst * 2 * kChunkK) >> gshift, g1 = ((pst * 2 + 1) * kChunkK) >> gshift;
-        s.sa0 = __ldg(psA + g0);
-        s.sa1 = __ldg(psA + g1);
-        s.sb0 = __ldg(psB + g0);
-        s.sb1 = __ldg(psB + g1);
-        s.za0 = __ldg(pzA + g0);
-        s.za1 = __ldg(pzA + g1);
-        s.zb0 = __ldg(pzB + g0);
-        s.zb1 = __ldg(pzB + g1);
-      } else {
-        s.sa0 = s.sa1 = __ldg(psA);
-        s.sb0 = s.sb1 = __ldg(psB);
-      }
-      ++pu;
-      if (++pst == spt) {
-        pst = 0;
-        ++pitem;
-        if (pu < end) set_prow(pitem);
-      }
-    }
-  };
-  Step ring[kD];
-#pragma unroll
-  for (int j = 0; j < kD; ++j) fetch(ring[j]);
+  if (lane == 0) {
+    for (int i = 0; i < kS; ++i) mbar_init(bars + i, 1);
+    fence_mbar_init();
+  }
+  // everything above overlaps the previous kernel (programmatic dependent launch); no
+  // global memory is touched before this wait
+  grid_dep_wait();
+  if (lane == 0) {
+    for (int u = 0; u < kS - 1 && u < total; ++u) issue(u);
+  }
+  __syncwarp();
 
-  // ---- main cursor ----
-  int64_t item = beg / spt;
-  int st = (int)(beg % spt);
+  // ---- consumer side ----
+  uint32_t item = beg / spt;
+  uint32_t st = beg - item * spt;
   const __nv_bfloat16* xrow[MT];  // activation row tt * 8 + g8 of the item's batch (clamped)
   auto set_xrow = [&]() {
-    const int64_t b0 = (item / tiles) * kBatch;
+    const int64_t b0 = (int64_t)(item / tiles) * kBatch;
 #pragma unroll
     for (int tt = 0; tt < MT; ++tt) xrow[tt] = p.x + imin64(b0 + tt * 8 + g8, M - 1) * K + cq * kPiece;
   };
@@ -693,20 +762,21 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM) k_gemv_fact(const Gemv
   float tot[MT][4];  // D fragments of the segment, scaled: rows g8 / g8 + 8, columns 2cq, 2cq+1
 #pragma unroll
   for (int tt = 0; tt < MT; ++tt) tot[tt][0] = tot[tt][1] = tot[tt][2] = tot[tt][3] = 0.0f;
-  bool seg_first = true;             // the segment holds this warp's first step
-  bool seg_from_start = (st == 0);   // the segment began at step 0 of its tile
-  int pend_tile[2] = {-1, -1};       // tiles cut by this warp's range boundaries
-  int npend = 0;
+  bool seg_first = true;            // the segment holds this warp's first step
+  bool seg_from_start = (st == 0);  // the segment began at step 0 of its tile
 
   // one chunk: tot += s (.) (W-chunk - z) x-chunk on the MMA
   auto chunk = [&](const uint4& wa, const uint4& wb, float sa, float sb, uint32_t za, uint32_t zb,
                    int kx) {
+    const __nv_bfloat16* xb[MT];
+#pragma unroll
+    for (int tt = 0; tt < MT; ++tt) xb[tt] = xrow[tt] + kx;
     uint32_t xr[MT][kXR];
 #pragma unroll
     for (int tt = 0; tt < MT; ++tt) {
 #pragma unroll
       for (int q = 0; q < kXR / 4; ++q) {
-        const uint4 v = ld_global_nc_v4(xrow[tt] + kx + q * 8);
+        const uint4 v = ld_global_nc_v4(xb[tt] + q * 8);
         if constexpr (F == Fmt::I8R) {
           xr[tt][4 * q + 0] = v.x;
           xr[tt][4 * q + 1] = v.y;
@@ -747,8 +817,8 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM) k_gemv_fact(const Gemv
           uint32_t da[4], db[4];
           const uint32_t a = (F == Fmt::I4R) ? (wA[i] ^ 0x88888888u) : wA[i];
           const uint32_t b = (F == Fmt::I4R) ? (wB[i] ^ 0x88888888u) : wB[i];
-          nib8_minus_zero<kBig>(a, zcA, zc2A, da);
-          nib8_minus_zero<kBig>(b, zcB, zc2B, db);
+          nib8_minus_zero<kBig>(a, zcA, zc2A, magic, da);
+          nib8_minus_zero<kBig>(b, zcB, zc2B, magic, db);
 #pragma unroll
           for (int tt = 0; tt < MT; ++tt) {
             mma_bf16_16816(acc[tt][0], da[0], db[0], da[1], db[1], xr[tt][4 * i],
@@ -782,68 +852,158 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM) k_gemv_fact(const Gemv
     }
   };
 
-  const int total = (int)(end - beg);
-  for (int u0 = 0; u0 < total; u0 += kD) {
-#pragma unroll
-    for (int j = 0; j < kD; ++j) {
-      if (u0 + j < total) {
-        const Step s = ring[j];
-        fetch(ring[j]);
-        const int kx = st * 2 * kChunkK;
-        chunk(s.a0, s.b0, s.sa0, s.sb0, s.za0, s.zb0, kx);
-        chunk(s.a1, s.b1, s.sa1, s.sb1, s.za1, s.zb1, kx + kChunkK);
-
-        // ---- end of a segment: the tile ends here, or this warp's range does ----
-        const bool tile_end = (st == spt - 1);
-        if (tile_end || u0 + j + 1 == total) {
-          const bool full_tile = seg_from_start && tile_end;
-          const int tile = (int)(item % tiles);
-          const int slot_id = seg_first ? 0 : 1;
-          const int64_t b0 = (item / tiles) * kBatch;
-#pragma unroll
-          for (int tt = 0; tt < MT; ++tt) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              // D fragment: i = 0, 1 -> row g8, columns 2cq, 2cq+1; i = 2, 3 -> row g8 + 8
-              const float v = tot[tt][i];
-              tot[tt][i] = 0.0f;
-              const int64_t m = b0 + tt * 8 + 2 * cq + (i & 1);
-              const int row = g8 + ((i >> 1) << 3);
-              const int64_t n = (int64_t)tile * kRows + row;
-              if (m < M) {
-                if (full_tile) {
-                  if (n < N) {
-                    const float bias = p.bias ? __bfloat162float(p.bias[n]) : 0.0f;
-                    p.y[m * N + n] = __float2bfloat16_rn(v + bias);
-                  }
-                } else {
-                  p.ws_part[((c * 2 + slot_id) * M + m) * kRows + row] = v;
-                }
-              }
-            }
-          }
-          if (!full_tile) pend_tile[npend++] = tile;
-          seg_first = false;
-          seg_from_start = true;
-        }
-
-        // ---- advance the main cursor ----
-        if (++st == spt) {
-          st = 0;
-          ++item;
-          if (u0 + j + 1 < total) set_xrow();
-        }
+  // lane-constant offsets inside a stage: rows A / B, 16-byte units cq and 4 + cq, stored
+  // at unit ^ (row mod 8) by the swizzle
+  const uint32_t swz = (uint32_t)(g8 & 7);
+  const uint32_t offA0 = g8 * 128 + (((uint32_t)cq ^ swz) << 4);
+  const uint32_t offA1 = g8 * 128 + (((uint32_t)(4 + cq) ^ swz) << 4);
+  const uint32_t w_base = smem_u32(wst), s_base = smem_u32(sst), z_base = smem_u32(zst);
+  int stage = 0;
+  uint32_t phase = 0;
+  for (int u = 0; u < total; ++u) {
+    if (!mbar_wait(bars + stage, phase)) {
+      // the copy never completed: record it, wait (bounded) for the other copies this
+      // warp has in flight, and give up on its range (the cluster barriers below are
+      // still reached by every thread)
+      if (lane == 0) {
+        set_dev_status(p.dev_status, WQ_DEV_TIMEOUT);
+        for (int v = u + 1; v < total && v <= u + kS - 2; ++v)
+          (void)mbar_wait(bars + v % kS, (uint32_t)(v / kS) & 1u);
       }
+      __syncwarp();
+      break;
+    }
+    // codes of rows A (g8) and B (g8 + 8 = 1024 bytes further)
+    const uint32_t wb = w_base + stage * kFactStageW;
+    const uint4 a0 = ld_shared_v4(wb + offA0);
+    const uint4 a1 = ld_shared_v4(wb + offA1);
+    const uint4 b0 = ld_shared_v4(wb + offA0 + 8 * 128);
+    const uint4 b1 = ld_shared_v4(wb + offA1 + 8 * 128);
+    float sa0, sa1, sb0, sb1;
+    uint32_t za0 = 0, za1 = 0, zb0 = 0, zb1 = 0;
+    const uint32_t sv = s_base + stage * kFactStageS;
+    if constexpr (F == Fmt::I4G) {
+      const int g0 = (int)((st * 2 * kChunkK) >> gshift), g1 = (int)(((st * 2 + 1) * kChunkK) >> gshift);
+      const uint32_t zv = z_base + stage * kFactStageZ;
+      const uint32_t s0 = (uint32_t)(g0 & 3) * 4, s1 = (uint32_t)(g1 - (g0 & ~3)) * 4;
+      const uint32_t z0 = (uint32_t)(g0 & 15), z1 = (uint32_t)(g1 - (g0 & ~15));
+      sa0 = ld_shared_f32(sv + g8 * 16 + s0);
+      sa1 = ld_shared_f32(sv + g8 * 16 + s1);
+      sb0 = ld_shared_f32(sv + (g8 + 8) * 16 + s0);
+      sb1 = ld_shared_f32(sv + (g8 + 8) * 16 + s1);
+      za0 = ld_shared_u8(zv + g8 * 16 + z0);
+      za1 = ld_shared_u8(zv + g8 * 16 + z1);
+      zb0 = ld_shared_u8(zv + (g8 + 8) * 16 + z0);
+      zb1 = ld_shared_u8(zv + (g8 + 8) * 16 + z1);
+    } else {
+      sa0 = sa1 = ld_shared_f32(sv + g8 * 4);
+      sb0 = sb1 = ld_shared_f32(sv + (g8 + 8) * 4);
+    }
+    // every lane has its data: the stage consumed in the previous step is free again
+    __syncwarp();
+    if (lane == 0 && u + kS - 1 < total) issue(u + kS - 1);
+    if (++stage == kS) {
+      stage = 0;
+      phase ^= 1u;
+    }
+
+    const int kx = (int)st * 2 * kChunkK;
+    chunk(a0, b0, sa0, sb0, za0, zb0, kx);
+    chunk(a1, b1, sa1, sb1, za1, zb1, kx + kChunkK);
+
+    // ---- end of a segment: the tile ends here, or this warp's range does ----
+    const bool tile_end = (st == spt - 1);
+    if (tile_end || u + 1 == total) {
+      if (seg_from_start && tile_end) {
+        emit_tile(p, item, tiles, kBatch, tot, g8, cq);
+      } else {
+        // a cut tile: park the partial; the warp holding the tile's last step (this
+        // one, if the tile ends here) adds the partials up later
+#pragma unroll
+        for (int tt = 0; tt < MT; ++tt)
+          *reinterpret_cast<float4*>(&s_part[warp][seg_first ? 0 : 1][lane][4 * tt]) =
+              make_float4(tot[tt][0], tot[tt][1], tot[tt][2], tot[tt][3]);
+        if (tile_end) close_item = (int)item;
+      }
+#pragma unroll
+      for (int tt = 0; tt < MT; ++tt) tot[tt][0] = tot[tt][1] = tot[tt][2] = tot[tt][3] = 0.0f;
+      seg_first = false;
+      seg_from_start = true;
+    }
+
+    // ---- advance the main cursor ----
+    if (++st == spt) {
+      st = 0;
+      ++item;
+      if (u + 1 < total) set_xrow();
     }
   }
+  }  // beg < end
 
-  finish_cut_tiles(p, c, G, items * spt, spt, pend_tile, npend, lane);
+  // ---- finish the cut tiles of the cluster ----
+  if (beg >= end) grid_dep_wait();  // (warps with work waited before their first load)
+  cluster_sync_all();
+  if (close_item >= 0) {
+    // contributors: the consecutive warps whose ranges meet the tile's units [t0, t1)
+    const Split sp = split();
+    const uint32_t t0 = (uint32_t)close_item * spt, t1 = t0 + spt;
+    uint32_t w0 = sp.wc;
+    while (w0 > 0 && sp.bound(w0) > t0) --w0;  // first warp whose range starts at or before t0
+    float tot[MT][4];
+#pragma unroll
+    for (int tt = 0; tt < MT; ++tt) tot[tt][0] = tot[tt][1] = tot[tt][2] = tot[tt][3] = 0.0f;
+    // four contributors at a time: their slots are read together, then added in order
+    uint32_t bw = sp.bound(w0);
+    for (uint32_t wb = w0; wb <= sp.wc; wb += 4) {
+      float4 v[4][MT];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t w = wb + q;
+        const uint32_t b0 = bw, b1 = (w <= sp.wc) ? sp.bound(w + 1) : b0;
+        bw = b1;
+        // empty ranges, and warps past the closer, add nothing
+        const bool on = (w <= sp.wc) && b0 < b1 && b1 > t0 && b0 < t1;
+        const int sid = (b0 >= t0) ? 0 : 1;  // the tile was the contributor's first segment?
+        const uint32_t rank = w / kWarps, ww = w % kWarps;
+#pragma unroll
+        for (int tt = 0; tt < MT; ++tt)
+          v[q][tt] = on ? ld_shared_cluster_f4(
+                              map_shared_rank(smem_u32(&s_part[ww][sid][lane][4 * tt]), rank))
+                        : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int tt = 0; tt < MT; ++tt) {
+          tot[tt][0] += v[q][tt].x;
+          tot[tt][1] += v[q][tt].y;
+          tot[tt][2] += v[q][tt].z;
+          tot[tt][3] += v[q][tt].w;
+        }
+    }
+    emit_tile(p, close_item, tiles, kBatch, tot, g8, cq);
+  }
+  // no CTA leaves while another may still read its slots
+  cluster_sync_all();
 }
 
-// Rows of the factored kernel hold whole steps (two 64-byte chunks).
-bool fact_shape_ok(Fmt f, int64_t K) {
-  const int64_t row_bytes = (f == Fmt::I8R) ? K : K / 2;
-  return row_bytes % (2 * kChunkBytes) == 0;
+// The factored kernel takes I4G with a group of at least 128 codes, I4R and I8R when
+// rows hold whole steps (two 64-byte chunks), there are at least 16 rows, the (item,
+// step) units count in 31 bits, and the tensor maps' rules hold: 16-byte aligned bases,
+// row strides a multiple of 16 bytes (for I4G zero points: K / G a multiple of 16).
+bool fact_ok(Fmt f, const GemvParams& p) {
+  const int64_t row_bytes = (f == Fmt::I8R) ? p.K : p.K / 2;
+  if (row_bytes % (2 * kChunkBytes) != 0 || p.N < kRows) return false;
+  const int64_t batch = (p.M <= 8) ? 8 : 16;
+  const int64_t items = ((p.N + kRows - 1) / kRows) * ((p.M + batch - 1) / batch);
+  if (items * (row_bytes / (2 * kChunkBytes)) >= (int64_t(1) << 31)) return false;
+  if ((reinterpret_cast<uintptr_t>(p.w) | reinterpret_cast<uintptr_t>(p.scale)) % 16 != 0)
+    return false;
+  if (f == Fmt::I4G) {
+    if (p.group < 128 || (p.K / p.group) % 16 != 0) return false;
+    if (reinterpret_cast<uintptr_t>(p.zero) % 16 != 0) return false;
+  }
+  return true;
 }
 
 // ------------------------------------------------------------------ host side
@@ -856,10 +1016,82 @@ cudaError_t launch_t(const GemvParams& p, int grid, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// The factored kernel runs in clusters of kFactCluster CTAs, as many clusters as fit on
+// the GPU at once (one wave), never more than there are items.
+constexpr int kFactMinSteps = 2;
+constexpr int kMaxDevicesGemv = 64;
+
 template <Fmt F, int MT>
-cudaError_t launch_fact(const GemvParams& p, int grid, cudaStream_t stream) {
-  k_gemv_fact<F, MT><<<grid, kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+cudaError_t launch_fact(const GemvParams& p, cudaStream_t stream) {
+  static int active[kMaxDevicesGemv] = {0};  // co-resident clusters a device (0: unknown)
+  static std::atomic<bool> smem_set{false};
+  if (!smem_set.load(std::memory_order_acquire)) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        k_gemv_fact<F, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kFactSmemBytes);
+    if (e != cudaSuccess) return e;
+    smem_set.store(true, std::memory_order_release);
+  }
+  // tensor maps of codes, scales and zero points
+  FactMaps maps;
+  const int64_t row_bytes = (F == Fmt::I8R) ? p.K : p.K / 2;
+  if (!encode_tensor_map_2d(&maps.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t*>(p.w),
+                            (uint64_t)row_bytes, (uint64_t)p.N, (uint64_t)row_bytes, 2 * kChunkBytes,
+                            kRows, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  if constexpr (F == Fmt::I4G) {
+    const uint64_t gpr = (uint64_t)(p.K / p.group);
+    if (!encode_tensor_map_2d(&maps.s, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, const_cast<float*>(p.scale),
+                              gpr, (uint64_t)p.N, gpr * 4, 4, kRows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_tensor_map_2d(&maps.z, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t*>(p.zero),
+                              gpr, (uint64_t)p.N, gpr, 16, kRows, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+  } else {
+    const uint64_t stride = ((uint64_t)p.N * 4 + 15) & ~uint64_t(15);
+    if (!encode_tensor_map_2d(&maps.s, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, const_cast<float*>(p.scale),
+                              (uint64_t)p.N, 1, stride, kRows, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+    maps.z = maps.s;  // unused
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevicesGemv) dev = 0;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kFactCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  // programmatic dependent launch: the prologue overlaps the previous kernel's tail; the
+  // kernel waits for it (griddepcontrol.wait) before touching global memory
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kFactSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (active[dev] == 0) {
+    cfg.gridDim = dim3(kFactCluster * kNumSMsFallback);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, k_gemv_fact<F, MT>, &cfg) != cudaSuccess || n <= 0) {
+      (void)cudaGetLastError();
+      n = kNumSMsFallback * kBlocksPerSM / kFactCluster;
+    }
+    active[dev] = n;
+  }
+  constexpr int64_t kBatch = 8 * MT;
+  const int64_t items = ((p.N + kRows - 1) / kRows) * ((p.M + kBatch - 1) / kBatch);
+  // at least kFactMinSteps steps a warp on average: fewer, fuller warps beat many idle
+  // ones whose cut tiles would need long reductions
+  const int64_t units = items * (row_bytes / (2 * kChunkBytes));
+  int64_t cap = std::min<int64_t>(active[dev], std::max<int64_t>(1, units / (kFactWarps * kFactMinSteps)));
+  if (const char* env = std::getenv("WQ_GEMV_CLUSTERS")) {  // tuning and test knob
+    const int v = std::atoi(env);
+    if (v >= 1) cap = v;
+  }
+  const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(cap, items));
+  cfg.gridDim = dim3((unsigned)(clusters * kFactCluster));
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, k_gemv_fact<F, MT>, p, maps);
 }
 
 // I4G with a group of at least 128 codes, I4R, I8R: the factored kernel (warp MMA,
@@ -868,8 +1100,8 @@ cudaError_t launch_fact(const GemvParams& p, int grid, cudaStream_t stream) {
 template <Fmt F>
 cudaError_t launch_f(const GemvParams& p, int64_t rows, int grid, cudaStream_t stream) {
   if constexpr (F != Fmt::MXFP4) {
-    if ((F != Fmt::I4G || p.group >= 128) && fact_shape_ok(F, p.K))
-      return rows <= 8 ? launch_fact<F, 1>(p, grid, stream) : launch_fact<F, 2>(p, grid, stream);
+    if (fact_ok(F, p))
+      return rows <= 8 ? launch_fact<F, 1>(p, stream) : launch_fact<F, 2>(p, stream);
   }
   if (rows <= 1) return launch_t<F, 1, true>(p, grid, stream);
   if (rows <= 2) return launch_t<F, 2, true>(p, grid, stream);
