@@ -11,7 +11,10 @@ CUDA graph; CUDA events between the graphs time each kind.
 Reported: value = algorithmic HBM GB/s of the whole step (bytes of packed weights, f32
 scales, u8 zeros, bf16 x and y), roofline of the dominant kernel against the measured
 copy bandwidth, an end-to-end figure through the public API with host buffers, and the
-CPU oracle's throughput on a bounded sample of the same work.
+CPU oracle's throughput on a bounded sample of the same work.  Beside it, the second half
+of the metric: the seven projections at M = 2048 on the tensor-core GEMM (TFLOP/s and the
+dominant kernel against the measured bf16 peak) and an M sweep of the gate projection
+(M = 1 .. 2048) across both regimes.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 """
@@ -40,6 +43,17 @@ WORKLOAD = "llama-3.1-8b decode, 7 projections x 32 layers, W4A16 group 128, M=1
 def proj_bytes(n: int, k: int, m: int = 1) -> int:
     """Algorithmic bytes of one projection: packed codes + f32 scale + u8 zero + x + y."""
     return n * k // 2 + n * (k // GROUP) * 5 + 2 * m * k + 2 * m * n
+
+
+def load_traffic(key: str):
+    """DRAM bytes a launch measured by ncu for this kernel and shape (profiles/traffic.json),
+    or None when not captured for the kernel as it stands."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            return json.load(f).get(key)
+    except (OSError, ValueError):
+        return None
 
 
 def load_peaks() -> dict:
@@ -163,6 +177,93 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------------------- GPU leg
+PREFILL_M = 2048
+SWEEP_M = (1, 4, 16, 64, 128, 512, 2048)
+
+
+def time_rotating(fn, reps: int, stream) -> float:
+    """Mean device time (us) of fn(i) for i = 0..reps-1 after two warm-up calls; callers
+    rotate through per-layer weights and inputs, more bytes than L2 holds."""
+    import torch
+
+    with torch.cuda.stream(stream):
+        fn(0)
+        fn(1)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(reps):
+            fn(i)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / reps
+
+
+def run_prefill(dev, weights, layers, peaks, stream):
+    """Tensor-core regime: the seven projections at M = 2048 (one launch each, per-layer
+    weights and activations in rotation), and an M sweep on the gate projection."""
+    import torch
+
+    import weight_only_quantized_linear_gb300 as wq
+    from weight_only_quantized_linear_gb300 import synth
+
+    names = synth.LLAMA_ORDER
+    reps = max(4, layers)
+    xs = {k: [synth.normal_bf16((PREFILL_M, k), seed=50 + i, device="cpu").to(dev) for i in range(min(layers, 8))]
+          for k in (4096, 14336)}
+    per = {}
+    tot_flops = 0.0
+    tot_us = 0.0
+    for n in names:
+        N, K = synth.LLAMA_PROJ[n]
+        y = torch.empty((PREFILL_M, N), dtype=torch.bfloat16, device=dev)
+
+        def call(i, n=n, K=K, y=y):
+            p_, s_, z_ = weights[i % layers][n]
+            wq.wq_linear_int4_groups(xs[K][i % len(xs[K])], p_, s_, z_, None, GROUP, y=y, stream=stream)
+
+        us = time_rotating(call, reps, stream)
+        fl = 2.0 * PREFILL_M * N * K
+        per[n] = {"us_per_launch": round(us, 2), "tflops": round(fl / us / 1e6, 1)}
+        tot_flops += fl
+        tot_us += us
+    dom = max(names, key=lambda n: per[n]["us_per_launch"])
+    dN, dK = synth.LLAMA_PROJ[dom]
+    dom_tf = 2.0 * PREFILL_M * dN * dK / per[dom]["us_per_launch"] / 1e6
+    peak = peaks["bf16_tflops"]
+    prefill = {
+        "M": PREFILL_M, "tflops": round(tot_flops / tot_us / 1e6, 1),
+        "frac_of_bf16_peak": round(tot_flops / tot_us / 1e6 / peak, 4),
+        "us_per_layer": round(tot_us, 2), "per_projection": per,
+        "roofline": {"bound": "tensor", "achieved": round(dom_tf, 1), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(dom_tf / peak, 4), "traffic": load_traffic(f"prefill {dN}x{dK} M={PREFILL_M}"),
+                     "kernel": f"k_gemm_w4g_tc on {dom} {dN}x{dK}, M={PREFILL_M}",
+                     "flops_per_launch": 2 * PREFILL_M * dN * dK,
+                     "peak_source": peaks["source"] + " (bf16_tflops, burst: each launch timed alone)"},
+        "how": "CUDA events over launches rotating through 32 layers' weights (and 8 activation sets)",
+    }
+    # M sweep on the gate projection (decode GEMV below M = 32, tensor-core GEMM from 32 on)
+    N, K = synth.LLAMA_PROJ["gate"]
+    sweep = {}
+    for M in SWEEP_M:
+        xm = [x[:M].contiguous() for x in xs[K]]
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        wsb = wq.wq_linear_int4_groups_workspace(M, N, K, GROUP)
+        ws = [wq.alloc_workspace(wsb, dev) for _ in range(layers)] if wsb else [None] * layers
+
+        def call(i, M=M, xm=xm, y=y, ws=ws):
+            p_, s_, z_ = weights[i % layers]["gate"]
+            wq.wq_linear_int4_groups(xm[i % len(xm)], p_, s_, z_, None, GROUP, y=y, workspace=ws[i % layers],
+                                     stream=stream)
+
+        us = time_rotating(call, reps, stream)
+        sweep[str(M)] = {"us": round(us, 2), "gbs": round(proj_bytes(N, K, M) / (us * 1e-6) / 1e9, 1),
+                         "tflops": round(2.0 * M * N * K / us / 1e6, 2),
+                         "regime": "decode GEMV (warp MMA)" if M < 32 else "tcgen05 GEMM"}
+    return prefill, sweep
+
+
 def build_weights(dev, layers: int, seed0: int = 1000):
     """Per layer and projection: packed u8 [N, K/2], scale f32 [N, K/G], zero u8 [N, K/G]."""
     import torch
@@ -273,6 +374,14 @@ def run_gpu(args):
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
+
+    # ---------------- tensor-core regime (M = 2048) and the M sweep ----------------
+    prefill = sweep = clk_prefill = None
+    if not args.no_prefill:
+        clocks_p = ClockSampler(dev.index if dev.index is not None else 0)
+        clocks_p.start()
+        prefill, sweep = run_prefill(dev, weights, layers, peaks, stream)
+        clk_prefill = clocks_p.stop()
     total_ms = t_start.elapsed_time(t_end)
     if world > 1:
         t = torch.tensor([total_ms], device=dev)
@@ -294,14 +403,7 @@ def run_gpu(args):
     dN, dK = synth.LLAMA_PROJ[dom]
     dom_us = per_kind[dom]["us_per_launch"]
     achieved = proj_bytes(dN, dK) / (dom_us * 1e-6) / 1e9
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(prof):
-        try:
-            with open(prof) as f:
-                traffic = json.load(f).get(dom)
-        except (OSError, ValueError):
-            traffic = None
+    traffic = load_traffic(f"decode {dN}x{dK}")
 
     # ---------------- end to end through the public API, host buffers ----------------
     x_host = {k: v.cpu().pin_memory() for k, v in xs.items()}
@@ -353,10 +455,44 @@ def run_gpu(args):
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
             "cpu_baseline": cpu,
+            "prefill_m2048": prefill,
+            "m_sweep_gate": sweep,
+            "clocks_prefill": clk_prefill,
         }
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
+    return 0
+
+
+def run_profile_case(args):
+    """A few launches of one kernel on one projection, for profiler captures: decode_gate /
+    decode_down (M = 1, workspace on, as timed above) or prefill_gate (M = 2048)."""
+    import torch
+
+    import weight_only_quantized_linear_gb300 as wq
+    from weight_only_quantized_linear_gb300 import synth
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    wq.build()
+    kind, proj = args.profile_case.split("_")
+    N, K = synth.LLAMA_PROJ[proj]
+    M = 1 if kind == "decode" else PREFILL_M
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    w = synth.weight_f32(N, K, seed=1000, outlier_frac=0.001, device=dev)
+    codes, scale, zero = wq.wq_quantize_groups(w, GROUP, 4, wq.WQ_ASYM, dev_status=st)
+    packed = wq.wq_pack_int4(codes, True, dev_status=st)
+    del w, codes
+    x = synth.normal_bf16((M, K), seed=5, device="cpu").to(dev)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    ws = wq.alloc_workspace(wq.wq_linear_int4_groups_workspace(M, N, K, GROUP), dev)
+    for _ in range(3):
+        wq.wq_linear_int4_groups(x, packed, scale, zero, None, GROUP, y=y, workspace=ws, dev_status=st)
+    torch.cuda.synchronize()
+    if int(st.item()) != 0:
+        raise RuntimeError(f"device status {int(st.item())}")
+    print(f"profile case {args.profile_case}: M={M} N={N} K={K}, 3 launches")
     return 0
 
 
@@ -369,9 +505,14 @@ def main():
     ap.add_argument("--layers", type=int, default=LAYERS)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--profile-case", choices=["decode_gate", "decode_down", "prefill_gate"],
+                    help="run three launches of one kernel (for profiler captures) and exit")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.profile_case:
+        return run_profile_case(args)
     return run_gpu(args)
 
 
