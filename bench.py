@@ -13,8 +13,9 @@ scales, u8 zeros, bf16 x and y), roofline of the dominant kernel against the mea
 copy bandwidth, an end-to-end figure through the public API with host buffers, and the
 CPU oracle's throughput on a bounded sample of the same work.  Beside it, the second half
 of the metric: the seven projections at M = 2048 on the tensor-core GEMM (TFLOP/s and the
-dominant kernel against the measured bf16 peak) and an M sweep of the gate projection
-(M = 1 .. 2048) across both regimes.
+dominant kernel against the measured bf16 peak), an M sweep of the gate projection
+(M = 1 .. 2048) across both regimes, and the per-row int8 / int4 and MXFP4-experts
+variants at their configurations (GB/s against the HBM peak).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 """
@@ -264,6 +265,149 @@ def run_prefill(dev, weights, layers, peaks, stream):
     return prefill, sweep
 
 
+def run_variants(dev, peaks, stream):
+    """The format variants at their configurations: per-row int8 and int4 (M = 1, 8, 16 on
+    14336 x 4096 and 4096 x 14336) and MXFP4 experts in the shared-input form (E = 32,
+    K = 2880, N = 5760 and 2880, top-4 of 32, R = 1, 8, 64).  Weight copies and routing
+    tables rotate so that every launch reads its bytes from HBM."""
+    import torch
+
+    import weight_only_quantized_linear_gb300 as wq
+    from weight_only_quantized_linear_gb300 import synth
+
+    hbm = peaks["hbm_gbs"]
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    rows = {}
+    for (N, K) in ((14336, 4096), (4096, 14336)):
+        i8, i4 = [], []
+        for c in range(8):
+            w = synth.weight_f32(N, K, seed=700 + c, device=dev)
+            if c < 4:
+                q, sc, _ = wq.wq_quantize_groups(w, K, 8, wq.WQ_SYM, dev_status=st)
+                i8.append((q, sc[:, 0].contiguous()))
+            q4, sc4, _ = wq.wq_quantize_groups(w, K, 4, wq.WQ_SYM, dev_status=st)
+            i4.append((wq.wq_pack_int4(q4, False, dev_status=st).view(torch.int8), sc4[:, 0].contiguous()))
+            del w
+        for M in (1, 8, 16):
+            x = synth.normal_bf16((M, K), seed=9, device="cpu").to(dev)
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            for bits, mats in ((8, i8), (4, i4)):
+                wsb = wq.wq_linear_rows_workspace(M, N, K, bits)
+                ws = [wq.alloc_workspace(wsb, dev) for _ in range(len(mats))] if wsb else [None] * len(mats)
+                fn = wq.wq_linear_int8_rows if bits == 8 else wq.wq_linear_int4_rows
+
+                def call(i, fn=fn, mats=mats, ws=ws, x=x, y=y):
+                    qq, ss = mats[i % len(mats)]
+                    fn(x, qq, ss, None, y=y, workspace=ws[i % len(mats)], stream=stream)
+
+                us = time_rotating(call, 32, stream)
+                nbytes = (N * K if bits == 8 else N * K // 2) + 4 * N + 2 * M * K + 2 * M * N
+                gbs = nbytes / (us * 1e-6) / 1e9
+                rows[f"int{bits} {N}x{K} M={M}"] = {"us": round(us, 2), "gbs": round(gbs, 1),
+                                                    "frac_of_hbm_peak": round(gbs / hbm, 4)}
+    mx = {}
+    E, K, S = 32, 2880, 4
+    for N in (5760, 2880):
+        copies = [synth.mxfp4_experts(E, N, K, seed=800 + c, device=dev) for c in range(2)]
+        for R in (1, 8, 64):
+            routes = [synth.routing_topk(R, E, S, seed=900 + R + j, device=dev)[0] for j in range(8)]
+            touched = sum(len(set(r.flatten().tolist())) for r in routes) / len(routes)
+            x = synth.normal_bf16((R, 1, K), seed=11, device="cpu").to(dev)
+            y = torch.empty((R, S, N), dtype=torch.bfloat16, device=dev)
+            wsb = wq.wq_mxfp4_experts_shared_workspace(R, S, E, N, K)
+            ws = wq.alloc_workspace(wsb, dev) if wsb else None
+
+            def call(i, copies=copies, routes=routes, x=x, y=y, ws=ws):
+                b_, s_ = copies[i % 2]
+                wq.wq_mxfp4_experts_shared(x, b_, s_, routes[i % 8], y=y, workspace=ws, stream=stream)
+
+            us = time_rotating(call, 32, stream)
+            nbytes = touched * N * K * (0.5 + 1 / 32) + 2 * R * K + 2 * R * S * N
+            gbs = nbytes / (us * 1e-6) / 1e9
+            mx[f"N={N} R={R}"] = {"us": round(us, 2), "experts_touched": round(touched, 2), "gbs": round(gbs, 1),
+                                  "frac_of_hbm_peak": round(gbs / hbm, 4)}
+    torch.cuda.synchronize()
+    if int(st.item()) != 0:
+        raise RuntimeError(f"quantize/pack device status {int(st.item())}")
+    return rows, mx
+
+
+def run_fused_decode(dev, weights, layers, xs, stream, steps, warmup):
+    """The decode step with the projections that share an input stored concatenated along
+    N, as serving engines store them: qkv [6144, K] and gate_up [28672, K], one launch
+    each, so 4 launches a layer (qkv, o, gate_up, down) instead of 7.  Same weights, same
+    bytes, same outputs (rows of y in projection order)."""
+    import torch
+
+    import weight_only_quantized_linear_gb300 as wq
+    from weight_only_quantized_linear_gb300 import synth
+
+    groups = (("qkv", ("q", "k", "v")), ("o", ("o",)), ("gate_up", ("gate", "up")), ("down", ("down",)))
+    fused = []
+    for l in range(layers):
+        lw = {}
+        for gname, parts in groups:
+            if len(parts) == 1:
+                lw[gname] = weights[l][parts[0]]
+            else:
+                lw[gname] = tuple(torch.cat([weights[l][p][i] for p in parts], dim=0) for i in range(3))
+        fused.append(lw)
+    shapes = {g: (sum(synth.LLAMA_PROJ[p][0] for p in parts), synth.LLAMA_PROJ[parts[0]][1])
+              for g, parts in groups}
+    ys = {(l, g): torch.empty((1, shapes[g][0]), dtype=torch.bfloat16, device=dev)
+          for l in range(layers) for g, _ in groups}
+    ws = {g: [wq.alloc_workspace(wq.wq_linear_int4_groups_workspace(1, *shapes[g], GROUP), dev)
+              for _ in range(layers)] for g, _ in groups}
+
+    def launch_kind(g):
+        K = shapes[g][1]
+        for l in range(layers):
+            p_, s_, z_ = fused[l][g]
+            wq.wq_linear_int4_groups(xs[K], p_, s_, z_, None, GROUP, y=ys[(l, g)], workspace=ws[g][l],
+                                     stream=stream)
+
+    with torch.cuda.stream(stream):
+        for g, _ in groups:
+            launch_kind(g)
+    torch.cuda.synchronize()
+    graphs = {}
+    for g, _ in groups:
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            launch_kind(g)
+        graphs[g] = gr
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(groups) + 1)] for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            for g, _ in groups:
+                graphs[g].replay()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for st in range(steps):
+            for i, (g, _) in enumerate(groups):
+                evs[st][i].record(stream)
+                graphs[g].replay()
+            evs[st][len(groups)].record(stream)
+        t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    step_bytes = sum(proj_bytes(*synth.LLAMA_PROJ[n]) for n in synth.LLAMA_ORDER) * layers
+    per = {}
+    for i, (g, _) in enumerate(groups):
+        us = sum(e[i].elapsed_time(e[i + 1]) for e in evs) / (steps * layers) * 1e3
+        per[g] = {"shape": f"{shapes[g][0]}x{shapes[g][1]}", "us_per_launch": round(us, 3),
+                  "gbs": round(proj_bytes(*shapes[g]) / (us * 1e-6) / 1e9, 1)}
+    del fused
+    return {"value": round(step_bytes / (ms * 1e-3) / 1e9, 1), "unit": UNIT, "ms_per_step": round(ms, 4),
+            "us_per_layer": round(ms * 1e3 / layers, 3), "launches_per_step": 4 * layers,
+            "per_launch": per,
+            "how": "q/k/v and gate/up weights concatenated along N (one launch each), 4 launches a layer; "
+                   "same bytes and outputs as the 7-launch step"}
+
+
 def build_weights(dev, layers: int, seed0: int = 1000):
     """Per layer and projection: packed u8 [N, K/2], scale f32 [N, K/G], zero u8 [N, K/G]."""
     import torch
@@ -375,13 +519,15 @@ def run_gpu(args):
         dist.barrier()
     clk = clocks.stop()
 
-    # ---------------- tensor-core regime (M = 2048) and the M sweep ----------------
-    prefill = sweep = clk_prefill = None
+    # ---------------- the other legs: fused decode step, M = 2048, M sweep, variants ----------------
+    prefill = sweep = rows_leg = mxfp4_leg = None
+    clocks_p = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks_p.start()
+    fused_leg = run_fused_decode(dev, weights, layers, xs, stream, max(10, min(args.steps, 500)), args.warmup)
     if not args.no_prefill:
-        clocks_p = ClockSampler(dev.index if dev.index is not None else 0)
-        clocks_p.start()
         prefill, sweep = run_prefill(dev, weights, layers, peaks, stream)
-        clk_prefill = clocks_p.stop()
+        rows_leg, mxfp4_leg = run_variants(dev, peaks, stream)
+    clk_other = clocks_p.stop()
     total_ms = t_start.elapsed_time(t_end)
     if world > 1:
         t = torch.tensor([total_ms], device=dev)
@@ -456,8 +602,11 @@ def run_gpu(args):
             "clocks": clk,
             "cpu_baseline": cpu,
             "prefill_m2048": prefill,
+            "decode_fused_qkv_gateup": fused_leg,
             "m_sweep_gate": sweep,
-            "clocks_prefill": clk_prefill,
+            "rows_int8_int4": rows_leg,
+            "mxfp4_experts_shared": mxfp4_leg,
+            "clocks_other_legs": clk_other,
         }
         print(json.dumps(line))
     if world > 1:
