@@ -219,10 +219,13 @@ def run_prefill(dev, weights, layers, peaks, stream):
     for n in names:
         N, K = synth.LLAMA_PROJ[n]
         y = torch.empty((PREFILL_M, N), dtype=torch.bfloat16, device=dev)
+        # split-K scratch for the shapes with fewer output tiles than SMs (k, v)
+        ws = wq.alloc_workspace(wq.wq_linear_int4_groups_workspace(PREFILL_M, N, K, GROUP), dev)
 
-        def call(i, n=n, K=K, y=y):
+        def call(i, n=n, K=K, y=y, ws=ws):
             p_, s_, z_ = weights[i % layers][n]
-            wq.wq_linear_int4_groups(xs[K][i % len(xs[K])], p_, s_, z_, None, GROUP, y=y, stream=stream)
+            wq.wq_linear_int4_groups(xs[K][i % len(xs[K])], p_, s_, z_, None, GROUP, y=y, workspace=ws,
+                                     stream=stream)
 
         us = time_rotating(call, reps, stream)
         fl = 2.0 * PREFILL_M * N * K

@@ -100,11 +100,14 @@ WQ_API int wq_version(void);
  *   bias    bf16 [N] or NULL
  *   y       bf16 [M, N]         (written; must not alias the inputs)
  *   group   G in {32, 64, 128, 256}; K % G == 0 (else WQ_ESHAPE)
- *   workspace / ws_bytes: optional scratch for splitting K across thread blocks.  Size
- *           it with wq_linear_int4_groups_workspace(); it must be zero-filled once when
- *           allocated (the kernels leave it zero-filled again on return).  Pass NULL /
- *           0 to run without cross-block split-K (correct, slower at small N).  Calls
- *           that share one workspace must not run concurrently on the GPU.
+ *   workspace / ws_bytes: optional scratch for splitting K across thread blocks (decode
+ *           regime: arrival counters and partial tiles; tensor-core regime, M > 16, for
+ *           shapes with fewer 256 x 256 output tiles than SMs: f32 partial sums of each
+ *           k range).  Size it with wq_linear_int4_groups_workspace(); it must be
+ *           zero-filled once when allocated (the kernels leave it zero-filled again on
+ *           return), 16-byte aligned (256 in the decode regime).  Pass NULL / 0 to run
+ *           without cross-block split-K (correct, slower at small N).  Calls that share
+ *           one workspace must not run concurrently on the GPU.
  * The result is exact up to f32 accumulation order: |y - y_exact| <= 2e-3 *
  * sum_k |x_k W-hat_k| + 1 bf16 ulp.
  * ------------------------------------------------------------------------------------ */

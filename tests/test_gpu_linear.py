@@ -300,3 +300,28 @@ def test_gemm_matches_gemv_path(cuda_device, monkeypatch):
     yr, ad = oracle.linear_int4_groups(bf16_bits(x.cpu()), packed, scale, zero, None, N, G)
     assert_within(y_tc, yr, ad, "tcgen05")
     assert_within(y_gemv, yr, ad, "gemv")
+
+
+@pytest.mark.parametrize("M,N,K,G", [(256, 256, 4096, 128), (300, 1000, 3072, 64), (64, 520, 2048, 32)])
+def test_gemm_split_k(cuda_device, M, N, K, G):
+    """Tensor-core shapes with fewer tiles than SMs split K across blocks through the
+    workspace; the split result matches the oracle and the unsplit launch, and the
+    workspace is left zero-filled."""
+    d = cuda_device
+    packed, scale, zero = make_i4g(N, K, G, seed=M + N)
+    x = synth.normal_bf16((M, K), seed=M)
+    b = synth.normal_bf16((N,), seed=N)
+    nbytes = wq.wq_linear_int4_groups_workspace(M, N, K, G)
+    assert nbytes > 0, "expected a split-K workspace for a shape with few tiles"
+    args = (dev(x, d), dev(packed, d), dev(scale, d), dev(zero, d), dev(b, d), G)
+    y_split = run_i4g(d, *args, use_ws=True)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=d)
+    y2 = torch.empty((M, N), dtype=torch.bfloat16, device=d)
+    wq.wq_linear_int4_groups(*args[:4], args[4], G, y=y2, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(ws.view(torch.int32).abs().sum().item()) == 0, "partials not cleared"
+    y_whole = run_i4g(d, *args, use_ws=False)
+    yr, ad = oracle.linear_int4_groups(bf16_bits(x), packed, scale, zero, bf16_bits(b), N, G)
+    assert_within(y_split, yr, ad, f"split M={M} N={N} K={K}")
+    assert_within(y_whole, yr, ad, f"unsplit M={M} N={N} K={K}")
+    assert torch.equal(y_split.view(torch.int16), y2.view(torch.int16))

@@ -121,7 +121,7 @@ WQ_API int wq_version(void) { return 100; }
 // ------------------------------------------------------------------ group-wise 4-bit
 WQ_API size_t wq_linear_int4_groups_workspace(int64_t M, int64_t N, int64_t K, int32_t group) {
   if (M <= 0 || N <= 0 || K <= 0 || group <= 0) return 0;
-  if (M > 16 && gemm_tc_supported(M, N, K, group)) return 0;
+  if (M > 16 && gemm_tc_supported(M, N, K, group)) return gemm_tc_ws_bytes(M, N, K, num_sms_current());
   if (M > 16) return 0;
   return gemv_ws_bytes(Fmt::I4G, M, N, K);
 }
@@ -142,7 +142,15 @@ WQ_API int wq_linear_int4_groups(const void* x, int64_t M, int64_t K, const uint
   if (M > 16 && gemm_tc_supported(M, N, K, group)) {
     GemmTcParams gp{static_cast<const __nv_bfloat16*>(x), M, N, K, packed, scale, zero, group,
                     static_cast<const __nv_bfloat16*>(bias), static_cast<__nv_bfloat16*>(y),
-                    dev_status};
+                    dev_status, nullptr, 1};
+    // split-K when the caller's workspace holds the partials (optional: without it the
+    // tiles run unsplit, with the same result up to f32 summation order)
+    const size_t need = gemm_tc_ws_bytes(M, N, K, num_sms_current());
+    if (need > 0 && workspace != nullptr && ws_bytes >= need) {
+      if (!aligned(workspace, 16)) return WQ_EALIGN;
+      gp.part = static_cast<float*>(workspace);
+      gp.splits = gemm_tc_splits(M, N, K, num_sms_current());
+    }
     return launch_gemm_tc(gp, num_sms_current(), s) == cudaSuccess ? WQ_OK : WQ_ECUDA;
   }
 
@@ -198,6 +206,10 @@ WQ_API int wq_linear_int4_groups_noalloc(const void* x, int64_t M, int64_t K,
   if (st != WQ_OK) return st;
   if (group != 32 && group != 64 && group != 128 && group != 256) return WQ_ESHAPE;
   if (K % group != 0) return WQ_ESHAPE;
+  // the tensor-core regime needs no scratch (split-K is only an option there)
+  if (M > 16 && gemm_tc_supported(M, N, K, group))
+    return wq_linear_int4_groups(x, M, K, packed, scale, zero, order, bias, N, group, y,
+                                 nullptr, 0, dev_status, stream);
   const size_t need = wq_linear_int4_groups_workspace(M, N, K, group);
   if (need == 0)  // this shape runs without scratch
     return wq_linear_int4_groups(x, M, K, packed, scale, zero, order, bias, N, group, y,

@@ -20,8 +20,12 @@
 //               K-major 128-byte-swizzled layout the MMA reads; after the last k step
 //               they read the accumulators back (tcgen05.ld), add the bias, round to
 //               bf16 and store y.
+// Shapes with fewer tiles than half the SMs are split along K (blockIdx.z): each block
+// stores its tile's f32 partial sums, and a second kernel adds the partials in split
+// order (deterministic), adds the bias and rounds to bf16.
 // Every wait is bounded; a timeout records WQ_DEV_TIMEOUT and the block winds down
 // after the MMAs it issued have completed, freeing its TMEM.
+#include <algorithm>
 #include <atomic>
 #include <cstdlib>
 
@@ -129,6 +133,7 @@ struct SharedTc {
 
 }  // namespace
 
+template <bool kSplit>
 __global__ void __launch_bounds__(kThreadsTc, 1)
     k_gemm_w4g_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap pmap,
                   const GemmTcParams p) {
@@ -145,7 +150,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const int64_t M = p.M, N = p.N, K = p.K;
   const int64_t m0 = (int64_t)blockIdx.x * kBM;
   const int64_t n0 = (int64_t)blockIdx.y * kBN;
-  const int nk = (int)((K + kBK - 1) / kBK);
+  // this block's k steps: range blockIdx.z of gridDim.z equal ranges
+  const int nk_all = (int)((K + kBK - 1) / kBK);
+  const int kb0 = (int)(((int64_t)blockIdx.z * nk_all) / gridDim.z);
+  const int nk = (int)(((int64_t)(blockIdx.z + 1) * nk_all) / gridDim.z) - kb0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStagesTc; ++s) {
@@ -178,8 +186,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
         if (*reinterpret_cast<volatile int*>(&sh->abort)) break;
         mbar_arrive_expect_tx(&sh->full_tma[s], kABytes + kPBytes);
-        tma_load_2d(stage_a(s), &xmap, &sh->full_tma[s], kb * kBK, (int32_t)m0, pol);
-        tma_load_2d(stage_p(s), &pmap, &sh->full_tma[s], kb * (kBK / 2), (int32_t)n0, pol);
+        tma_load_2d(stage_a(s), &xmap, &sh->full_tma[s], (kb0 + kb) * kBK, (int32_t)m0, pol);
+        tma_load_2d(stage_p(s), &pmap, &sh->full_tma[s], (kb0 + kb) * (kBK / 2), (int32_t)n0, pol);
       }
     }
   } else if (warp == 1) {
@@ -228,7 +236,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     auto load_meta = [&](int kb) -> Meta {
       Meta m{1.0f, 1.0f, 0u};
       if (kb >= nk) return m;
-      const int64_t g0 = imin64(((int64_t)kb * kBK) >> gshift, gpr - 1);
+      const int64_t g0 = imin64(((int64_t)(kb0 + kb) * kBK) >> gshift, gpr - 1);
       const int64_t g1 = imin64(g0 + 1, gpr - 1);
       m.s0 = __ldg(&p.scale[n * gpr + g0]);
       m.z = __ldg(&p.zero[n * gpr + g0]);
@@ -288,12 +296,25 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const int acc = (warp - 2) >> 2; // accumulator (activation rows 0..127 or 128..255)
     const int64_t m = m0 + acc * 128 + q * 32 + lane;
     const bool vec_ok = (N % 8 == 0) && ((reinterpret_cast<uintptr_t>(p.y) & 15) == 0);
+    constexpr bool split = kSplit;  // f32 partials to the workspace, no bias
 #pragma unroll 1
     for (int ch = 0; ch < kBN / 32; ++ch) {
       uint32_t r[32];
       tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + acc * kBN + ch * 32, r);
       const int64_t nb = n0 + ch * 32;
-      if (m < M && nb < N) {
+      if (split && m < M && nb < N) {
+        // f32 partial sums of this k range, no bias (the reduction adds it)
+        float* dst = p.part + ((int64_t)blockIdx.z * M + m) * N + nb;
+        if (N % 4 == 0 && nb + 32 <= N) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            *reinterpret_cast<float4*>(dst + 4 * i) =
+                make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                            __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+        } else {
+          for (int i = 0; i < 32 && nb + i < N; ++i) dst[i] = __uint_as_float(r[i]);
+        }
+      } else if (m < M && nb < N) {
         float v[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -326,7 +347,84 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   }
 }
 
+// y[m, n] = bf16(sum over splits z, in order, of part[z, m, n] + bias[n]).  The partials are
+// zeroed as they are read: the workspace is left zero-filled, as every entry point of
+// the library leaves it.  Grid: (column chunks of 4 x 256, rows); all splits' loads of a
+// thread are issued before any of its stores.
+constexpr int kMaxSplits = 8;
+
+__global__ void __launch_bounds__(256) k_splitk_reduce(float* __restrict__ part, int splits,
+                                                       int64_t M, int64_t N,
+                                                       const __nv_bfloat16* __restrict__ bias,
+                                                       __nv_bfloat16* __restrict__ y) {
+  const int64_t m = blockIdx.y;
+  const int64_t n = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (n >= N) return;
+  const int64_t total = M * N;
+  float* const row = part + m * N + n;
+  float v[kMaxSplits][4];
+  if (N % 4 == 0) {
+#pragma unroll
+    for (int z = 0; z < kMaxSplits; ++z) {
+      if (z < splits) {
+        const float4 u = __ldcg(reinterpret_cast<const float4*>(row + (int64_t)z * total));
+        v[z][0] = u.x;
+        v[z][1] = u.y;
+        v[z][2] = u.z;
+        v[z][3] = u.w;
+      }
+    }
+#pragma unroll
+    for (int z = 0; z < kMaxSplits; ++z)
+      if (z < splits)
+        __stcg(reinterpret_cast<float4*>(row + (int64_t)z * total), make_float4(0.f, 0.f, 0.f, 0.f));
+  } else {
+    // ragged rows: element by element (the last chunk may be short)
+#pragma unroll
+    for (int z = 0; z < kMaxSplits; ++z) {
+      if (z < splits) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          v[z][j] = 0.0f;
+          if (n + j < N) {
+            v[z][j] = row[(int64_t)z * total + j];
+            row[(int64_t)z * total + j] = 0.0f;
+          }
+        }
+      }
+    }
+  }
+  float acc[4] = {v[0][0], v[0][1], v[0][2], v[0][3]};
+#pragma unroll
+  for (int z = 1; z < kMaxSplits; ++z)
+    if (z < splits)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[j] += v[z][j];
+  __nv_bfloat16* const out = y + m * N + n;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if (n + j < N) {
+      float o = acc[j];
+      if (bias) o += __bfloat162float(bias[n + j]);
+      out[j] = __float2bfloat16_rn(o);
+    }
+  }
+}
+
 // ------------------------------------------------------------------ host side
+int gemm_tc_splits(int64_t M, int64_t N, int64_t K, int num_sms) {
+  const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
+  const int64_t nk = (K + kBK - 1) / kBK;
+  if (tiles * 2 > num_sms) return 1;
+  // as many k ranges as fill the SMs, each of at least 8 k steps, at most 8 ranges
+  return (int)std::max<int64_t>(1, std::min<int64_t>({num_sms / tiles, nk / 8, (int64_t)kMaxSplits}));
+}
+
+size_t gemm_tc_ws_bytes(int64_t M, int64_t N, int64_t K, int num_sms) {
+  const int s = gemm_tc_splits(M, N, K, num_sms);
+  return s > 1 ? (size_t)s * (size_t)M * (size_t)N * 4 : 0;
+}
+
 bool gemm_tc_supported(int64_t M, int64_t N, int64_t K, int32_t group) {
   if (const char* env = std::getenv("WQ_GEMM_MIN_M")) {  // tuning knob for the crossover
     if (M < std::atoll(env)) return false;
@@ -339,7 +437,6 @@ bool gemm_tc_supported(int64_t M, int64_t N, int64_t K, int32_t group) {
 }
 
 cudaError_t launch_gemm_tc(const GemmTcParams& p, int num_sms, cudaStream_t stream) {
-  (void)num_sms;
   CUtensorMap xmap, pmap;
   if (!encode_tensor_map_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                             const_cast<__nv_bfloat16*>(p.x), (uint64_t)p.K, (uint64_t)p.M,
@@ -356,12 +453,29 @@ cudaError_t launch_gemm_tc(const GemmTcParams& p, int num_sms, cudaStream_t stre
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
   if (!(attr_set.load(std::memory_order_acquire) & bit)) {
-    e = cudaFuncSetAttribute(k_gemm_w4g_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(k_gemm_w4g_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_gemm_w4g_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
     if (e != cudaSuccess) return e;
     attr_set.fetch_or(bit, std::memory_order_release);
   }
-  const dim3 grid((unsigned)((p.M + kBM - 1) / kBM), (unsigned)((p.N + kBN - 1) / kBN));
-  k_gemm_w4g_tc<<<grid, kThreadsTc, smem, stream>>>(xmap, pmap, p);
+  const int splits = (p.part != nullptr) ? std::max(1, (int)p.splits) : 1;
+  GemmTcParams q = p;
+  if (splits == 1) q.part = nullptr;
+  const dim3 grid((unsigned)((p.M + kBM - 1) / kBM), (unsigned)((p.N + kBN - 1) / kBN),
+                  (unsigned)splits);
+  if (splits == 1)
+    k_gemm_w4g_tc<false><<<grid, kThreadsTc, smem, stream>>>(xmap, pmap, q);
+  else
+    k_gemm_w4g_tc<true><<<grid, kThreadsTc, smem, stream>>>(xmap, pmap, q);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || splits == 1) return e;
+  // splits > 1 only with at most num_sms / 2 tiles, so M <= 256 * num_sms / 2 rows: within
+  // the grid's y limit
+  const dim3 rgrid((unsigned)((p.N + 1023) / 1024), (unsigned)p.M);
+  k_splitk_reduce<<<rgrid, 256, 0, stream>>>(q.part, splits, p.M, p.N, p.bias, p.y);
   return cudaGetLastError();
 }
 

@@ -81,8 +81,14 @@ struct GemmTcParams {
   const __nv_bfloat16* bias;
   __nv_bfloat16* y;        // [M, N]
   int32_t* dev_status;
+  float* part;             // split-K partials [splits, M, N] f32, or NULL (no split)
+  int32_t splits;          // k ranges a tile is cut into (1: no split)
 };
 bool gemm_tc_supported(int64_t M, int64_t N, int64_t K, int32_t group);
+// Split-K for shapes with fewer tiles than SMs: the number of k ranges, and the
+// workspace (f32 partials) it needs; 1 and 0 when the shape has tiles enough.
+int gemm_tc_splits(int64_t M, int64_t N, int64_t K, int num_sms);
+size_t gemm_tc_ws_bytes(int64_t M, int64_t N, int64_t K, int num_sms);
 cudaError_t launch_gemm_tc(const GemmTcParams& p, int num_sms, cudaStream_t stream);
 
 // Tensor-map encoding through the driver entry point (no link-time libcuda).
