@@ -453,6 +453,9 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     wq.build()
+    # decode serving: weights are written once at load time and never during a step, so
+    # each launch may start streaming its weights while the previous one finishes
+    wq.wq_set_static_weights(True)
     peaks = load_peaks()
 
     layers = args.layers
@@ -590,7 +593,8 @@ def run_gpu(args):
             "data": "synthetic",
             "config": {"workload": WORKLOAD, "M": 1, "group": GROUP, "layers": layers,
                        "bytes_per_step": step_bytes, "l2": "inputs larger than L2 (3.77 GB of weights a step)",
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "static_weights": "wq_set_static_weights(1): weights are load-time constants"},
             "frac_of_hbm_peak": round(value / world / peaks["hbm_gbs"], 4),
             "us_per_layer": round(ms_per_step * 1e3 / layers, 3),
             "per_projection": per_kind,

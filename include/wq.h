@@ -123,6 +123,23 @@ WQ_API size_t wq_linear_int4_groups_workspace(int64_t M, int64_t N, int64_t K,
                                               int32_t group);
 
 /* ------------------------------------------------------------------------------------
+ * Declare the weights immutable (the source pages have no counterpart: a launch-order
+ * promise made by the caller, not an operation of the method).
+ *
+ * on != 0: the caller promises that no GPU work writes the packed codes, scales or zero
+ * points passed to the decode-regime linears (wq_linear_int4_groups and its _noalloc
+ * variant with M <= 16, wq_linear_int8_rows, wq_linear_int4_rows) while a call that
+ * reads them may run, in particular not the kernel issued just before the call on its
+ * stream.  Weights loaded once and synchronized before serving satisfy it.  The decode
+ * kernel then starts streaming its first weight stages while the previous kernel of the
+ * stream is still running (programmatic dependent launch); activations, outputs and the
+ * workspace are still read and written only after that kernel has completed.
+ * on == 0 (the default): nothing is read before the previous kernel has completed.
+ * Process-wide; applies to launches issued after the call.  Returns WQ_OK.
+ * ------------------------------------------------------------------------------------ */
+WQ_API int wq_set_static_weights(int on);
+
+/* ------------------------------------------------------------------------------------
  * Allocation-free variant of wq_linear_int4_groups (the source pages have no
  * counterpart; it exists for callers of this library).
  *

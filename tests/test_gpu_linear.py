@@ -325,3 +325,35 @@ def test_gemm_split_k(cuda_device, M, N, K, G):
     assert_within(y_split, yr, ad, f"split M={M} N={N} K={K}")
     assert_within(y_whole, yr, ad, f"unsplit M={M} N={N} K={K}")
     assert torch.equal(y_split.view(torch.int16), y2.view(torch.int16))
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (5, 1000, 2048)])
+def test_static_weights_same_result(cuda_device, M, N, K):
+    """Streaming the weights before the previous kernel completes changes no bit of the
+    result: back-to-back calls on one stream, each right after a kernel that rewrites the
+    activations (which are read only after that kernel has completed)."""
+    d = cuda_device
+    G = 128
+    packed, scale, zero = make_i4g(N, K, G, seed=31)
+    x0 = dev(synth.normal_bf16((M, K), seed=32), d)
+    args = (dev(packed, d), dev(scale, d), dev(zero, d))
+    ws = wq.alloc_workspace(wq.wq_linear_int4_groups_workspace(M, N, K, G), d)
+    outs = []
+    for on in (False, True):
+        wq.wq_set_static_weights(on)
+        try:
+            x = x0.clone()
+            ys = []
+            for i in range(4):
+                x.copy_(x0 * float(i + 1))  # a kernel that writes the activations just before the call
+                y = torch.empty((M, N), dtype=torch.bfloat16, device=d)
+                wq.wq_linear_int4_groups(x, *args, None, G, y=y, workspace=ws)
+                ys.append(y)
+            torch.cuda.synchronize()
+            outs.append(torch.stack(ys))
+        finally:
+            wq.wq_set_static_weights(False)
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    x3 = (x0 * 4.0).cpu()
+    yr, ad = oracle.linear_int4_groups(bf16_bits(x3), packed, scale, zero, None, N, G)
+    assert_within(outs[1][3], yr, ad, "static weights, last call")

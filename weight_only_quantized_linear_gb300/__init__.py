@@ -33,6 +33,7 @@ SIGNATURES = {
     "wq_linear_int4_groups": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P, _P, _P, _I64, _I32, _P, _P, _SZ,
                                              _P, _P]),
     "wq_linear_int4_groups_workspace": (_SZ, [_I64, _I64, _I64, _I32]),
+    "wq_set_static_weights": (ctypes.c_int, [ctypes.c_int]),
     "wq_linear_int4_groups_noalloc": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P, _P, _P, _I64, _I32, _P,
                                                      _P, _P]),
     "wq_linear_int8_rows": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P, _I64, _P, _P, _SZ, _P, _P]),
@@ -126,6 +127,13 @@ def wq_linear_rows_workspace(M: int, N: int, K: int, bits: int) -> int:
 
 def wq_mxfp4_experts_shared_workspace(R: int, S: int, E: int, N: int, K: int) -> int:
     return int(lib().wq_mxfp4_experts_shared_workspace(R, S, E, N, K))
+
+
+def wq_set_static_weights(on: bool) -> None:
+    """Promise that the weights passed to the decode-regime linears are not written by GPU
+    work while calls read them (see wq.h): the decode kernel may then start streaming
+    them before the previous kernel of the stream has completed."""
+    _check(lib().wq_set_static_weights(1 if on else 0), "wq_set_static_weights")
 
 
 def alloc_workspace(nbytes: int, device) -> torch.Tensor | None:

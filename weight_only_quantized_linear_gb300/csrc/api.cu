@@ -118,6 +118,11 @@ WQ_API const char* wq_status_string(int status) {
 
 WQ_API int wq_version(void) { return 100; }
 
+WQ_API int wq_set_static_weights(int on) {
+  set_static_weights(on);
+  return WQ_OK;
+}
+
 // ------------------------------------------------------------------ group-wise 4-bit
 WQ_API size_t wq_linear_int4_groups_workspace(int64_t M, int64_t N, int64_t K, int32_t group) {
   if (M <= 0 || N <= 0 || K <= 0 || group <= 0) return 0;

@@ -741,11 +741,19 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     for (int i = 0; i < kS; ++i) mbar_init(bars + i, 1);
     fence_mbar_init();
   }
-  // everything above overlaps the previous kernel (programmatic dependent launch); no
-  // global memory is touched before this wait
-  grid_dep_wait();
-  if (lane == 0) {
-    for (int u = 0; u < kS - 1 && u < total; ++u) issue(u);
+  // everything above overlaps the previous kernel (programmatic dependent launch).  Before
+  // the wait, only the weights (codes, scales, zero points) may be read, and only when the
+  // caller has declared them immutable; activations, outputs and everything else wait.
+  if (p.weights_static) {
+    if (lane == 0) {
+      for (int u = 0; u < kS - 1 && u < total; ++u) issue(u);
+    }
+    grid_dep_wait();
+  } else {
+    grid_dep_wait();
+    if (lane == 0) {
+      for (int u = 0; u < kS - 1 && u < total; ++u) issue(u);
+    }
   }
   __syncwarp();
 
@@ -1111,6 +1119,13 @@ cudaError_t launch_f(const GemvParams& p, int64_t rows, int grid, cudaStream_t s
 
 }  // namespace
 
+namespace {
+std::atomic<int> g_static_weights{0};
+}  // namespace
+
+void set_static_weights(int on) { g_static_weights.store(on ? 1 : 0, std::memory_order_relaxed); }
+int static_weights() { return g_static_weights.load(std::memory_order_relaxed); }
+
 GemvPlan plan_gemv(Fmt f, int64_t M, int64_t N, int64_t K, int num_sms) {
   GemvPlan pl;
   const int ck = (f == Fmt::I8R) ? 64 : 128;
@@ -1137,6 +1152,7 @@ bool gemv_mxfp4_supported(int64_t R, int64_t S, int64_t E) {
 }
 
 cudaError_t launch_gemv(Fmt f, GemvParams p, const GemvPlan& pl, cudaStream_t stream) {
+  p.weights_static = static_weights();
   if (!pl.stream_k) {
     p.ws_cnt = nullptr;
     p.ws_part = nullptr;

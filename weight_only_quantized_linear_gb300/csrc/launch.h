@@ -31,6 +31,7 @@ struct GemvParams {
   float* ws_part;          // stream-K partial tiles [warps, 2, M, 16 rows]
   uint32_t* ws_cnt;        // stream-K arrival counters [tiles]
   int32_t* dev_status;
+  int32_t weights_static;  // the caller promises the weights are not written meanwhile
 };
 
 struct GemvPlan {
@@ -47,6 +48,11 @@ inline size_t ws_counter_bytes(int tiles) { return ((size_t)tiles * 4 + 255) & ~
 
 GemvPlan plan_gemv(Fmt f, int64_t M, int64_t N, int64_t K, int num_sms);
 cudaError_t launch_gemv(Fmt f, GemvParams p, const GemvPlan& plan, cudaStream_t stream);
+// Weights declared immutable by the caller (wq_set_static_weights): decode kernels may
+// start reading them before the previous kernel of the stream has completed.
+void set_static_weights(int on);
+int static_weights();
+
 // MXFP4 routing tables live in shared memory: bounded slot and expert counts.
 bool gemv_mxfp4_supported(int64_t R, int64_t S, int64_t E);
 
