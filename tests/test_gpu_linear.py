@@ -357,3 +357,19 @@ def test_static_weights_same_result(cuda_device, M, N, K):
     x3 = (x0 * 4.0).cpu()
     yr, ad = oracle.linear_int4_groups(bf16_bits(x3), packed, scale, zero, None, N, G)
     assert_within(outs[1][3], yr, ad, "static weights, last call")
+
+
+@pytest.mark.parametrize("xsmem", ["1", "0"])
+@pytest.mark.parametrize("M,N,K", [(1, 4096, 14336), (3, 1000, 4096), (8, 300, 2048)])
+def test_factored_activation_paths(cuda_device, monkeypatch, xsmem, M, N, K):
+    """Activations staged in shared memory (the default where two blocks an SM still fit,
+    with a three-stage ring at K = 14336) and read from global memory give results
+    within the tolerance."""
+    monkeypatch.setenv("WQ_GEMV_XSMEM", xsmem)
+    d = cuda_device
+    G = 128
+    packed, scale, zero = make_i4g(N, K, G, seed=K + M)
+    x = synth.normal_bf16((M, K), seed=M + 40)
+    y = run_i4g(d, dev(x, d), dev(packed, d), dev(scale, d), dev(zero, d), None, G)
+    yr, ad = oracle.linear_int4_groups(bf16_bits(x), packed, scale, zero, None, N, G)
+    assert_within(y, yr, ad, f"xsmem={xsmem} M={M} N={N} K={K}")

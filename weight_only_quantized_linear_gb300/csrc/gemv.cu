@@ -635,24 +635,30 @@ struct FactMaps {
   CUtensorMap z;  // I4G: zero points [N, K/G] u8, box {16, 16}
 };
 
-constexpr int kFactStages = 4;
 constexpr int kFactStageW = 2048;  // code bytes a stage (16 rows x 128)
 constexpr int kFactStageS = 256;   // scale bytes a stage (I4G: 16 rows x 4 groups)
 constexpr int kFactStageZ = 256;   // zero-point bytes a stage (16 rows x 16 groups)
+constexpr int kFactXPad = 64;      // bytes between staged activation rows (banks)
 // dynamic shared memory: codes (1024-byte aligned for the swizzle), scales, zero points,
-// barriers; plus slack for the alignment
-constexpr int kFactSmemBytes =
-    kWarps * kFactStages * (kFactStageW + kFactStageS + kFactStageZ + 8) + 1024;
+// barriers of kSD stages a warp; then the staged activations; plus slack for the alignment
+__host__ __device__ constexpr int fact_ring_bytes(int kSD) {
+  return kWarps * kSD * (kFactStageW + kFactStageS + kFactStageZ + 8);
+}
 
-template <Fmt F, int MT>
+// kSD: ring stages a warp.  kXS: activations staged once a block in shared memory, in the
+// order of the MMA fragments ([row][k / 128][(k / 8) % 4][(k / 32) % 4] 16-byte pieces
+// holding (x0, x4) (x1, x5) (x2, x6) (x3, x7)), so that a lane's B fragments are four
+// 16-byte shared loads a chunk, with no shuffles and no global-memory latency in the loop.
+template <Fmt F, int MT, int kSD, bool kXS>
 __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
-    k_gemv_fact(const GemvParams p, const __grid_constant__ FactMaps maps) {
+    k_gemv_fact(const GemvParams p, const __grid_constant__ FactMaps maps, const uint32_t xstride) {
   static_assert(F == Fmt::I4G || F == Fmt::I4R || F == Fmt::I8R, "affine formats only");
   constexpr int kPiece = piece_k<F>();   // k of a lane's 16 bytes
   constexpr int kChunkK = chunk_k<F>();  // k of a 64-byte chunk
   constexpr int kXR = kPiece / 2;        // bf16x2 registers of x a piece
   constexpr int kBatch = 8 * MT;         // activation rows an item
-  constexpr int kS = kFactStages;
+  constexpr int kS = kSD;
+  static_assert(!kXS || (F != Fmt::I8R && MT == 1), "staged activations: 4-bit formats, one batch");
   constexpr uint32_t kStageTx =
       kFactStageW + ((F == Fmt::I4G) ? kFactStageS + kFactStageZ : 16 * 4);
   // partial D fragments of cut tiles: [warp][first / last segment][lane][4 * MT]
@@ -709,8 +715,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
   const uint32_t magic = 0x43004300u | (uint32_t)(p.K >> 62);
   int close_item = -1;  // the cut tile this warp finishes after the cluster barrier
 
-  if (beg < end) {
-  const int total = (int)(end - beg);
+  const int total = beg < end ? (int)(end - beg) : 0;
   // ---- producer side: lane 0 fills stage (u mod kS) with the data of unit beg + u; its
   // cursor (tile row, step) advances one unit an issue ----
   const uint64_t pol_stream = l2_policy_evict_first();
@@ -744,19 +749,50 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
   // everything above overlaps the previous kernel (programmatic dependent launch).  Before
   // the wait, only the weights (codes, scales, zero points) may be read, and only when the
   // caller has declared them immutable; activations, outputs and everything else wait.
-  if (p.weights_static) {
-    if (lane == 0) {
-      for (int u = 0; u < kS - 1 && u < total; ++u) issue(u);
-    }
-    grid_dep_wait();
-  } else {
-    grid_dep_wait();
-    if (lane == 0) {
-      for (int u = 0; u < kS - 1 && u < total; ++u) issue(u);
-    }
+  if (p.weights_static && lane == 0) {
+    for (int u = 0; u < kS - 1 && u < total; ++u) issue(u);
+  }
+  grid_dep_wait();
+  if (!p.weights_static && lane == 0) {
+    for (int u = 0; u < kS - 1 && u < total; ++u) issue(u);
   }
   __syncwarp();
 
+  uint8_t* const xs = smem + fact_ring_bytes(kS);
+  if constexpr (kXS) {
+    // every thread of the block stages activations: eight independent 16-byte loads in
+    // flight a thread, then their permuted stores
+    const uint32_t k8n = (uint32_t)(K / 8);
+    const uint32_t xtotal = (uint32_t)M * k8n;
+    const uint32_t xbase = smem_u32(xs);
+    for (uint32_t base = 0; base < xtotal; base += 8 * kThreads) {
+      uint4 v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const uint32_t idx = base + q * kThreads + threadIdx.x;
+        if (idx < xtotal) {
+          const uint32_t m = idx / k8n, k8 = idx - m * k8n;
+          v[q] = ld_global_nc_v4(p.x + (int64_t)m * K + (int64_t)k8 * 8);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const uint32_t idx = base + q * kThreads + threadIdx.x;
+        if (idx < xtotal) {
+          const uint32_t m = idx / k8n, k8 = idx - m * k8n;
+          const uint32_t o0 = __byte_perm(v[q].x, v[q].z, 0x5410), o1 = __byte_perm(v[q].x, v[q].z, 0x7632);
+          const uint32_t o2 = __byte_perm(v[q].y, v[q].w, 0x5410), o3 = __byte_perm(v[q].y, v[q].w, 0x7632);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                           xbase + m * xstride + (k8 >> 4) * 256 + (k8 & 3) * 64 + ((k8 >> 2) & 3) * 16),
+                       "r"(o0), "r"(o1), "r"(o2), "r"(o3)
+                       : "memory");
+        }
+      }
+    }
+    __syncthreads();
+  }
+
+  if (beg < end) {
   // ---- consumer side ----
   uint32_t item = beg / spt;
   uint32_t st = beg - item * spt;
@@ -780,22 +816,36 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
 #pragma unroll
     for (int tt = 0; tt < MT; ++tt) xb[tt] = xrow[tt] + kx;
     uint32_t xr[MT][kXR];
-#pragma unroll
-    for (int tt = 0; tt < MT; ++tt) {
+    if constexpr (kXS) {
+      // row min(g8, M - 1), chunk kx / 128, this lane's 16 bytes of each word
+      const uint32_t xa = smem_u32(xs) + (uint32_t)imin64(g8, M - 1) * xstride + (uint32_t)cq * 16 +
+                          (uint32_t)(kx / kChunkK) * 256;
 #pragma unroll
       for (int q = 0; q < kXR / 4; ++q) {
-        const uint4 v = ld_global_nc_v4(xb[tt] + q * 8);
-        if constexpr (F == Fmt::I8R) {
-          xr[tt][4 * q + 0] = v.x;
-          xr[tt][4 * q + 1] = v.y;
-          xr[tt][4 * q + 2] = v.z;
-          xr[tt][4 * q + 3] = v.w;
-        } else {
-          // word q of the piece holds elements 8q..8q+7: pairs (8q + j, 8q + j + 4)
-          xr[tt][4 * q + 0] = __byte_perm(v.x, v.z, 0x5410);
-          xr[tt][4 * q + 1] = __byte_perm(v.x, v.z, 0x7632);
-          xr[tt][4 * q + 2] = __byte_perm(v.y, v.w, 0x5410);
-          xr[tt][4 * q + 3] = __byte_perm(v.y, v.w, 0x7632);
+        const uint4 v = ld_shared_v4(xa + q * 64);
+        xr[0][4 * q + 0] = v.x;
+        xr[0][4 * q + 1] = v.y;
+        xr[0][4 * q + 2] = v.z;
+        xr[0][4 * q + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int tt = 0; tt < MT; ++tt) {
+#pragma unroll
+        for (int q = 0; q < kXR / 4; ++q) {
+          const uint4 v = ld_global_nc_v4(xb[tt] + q * 8);
+          if constexpr (F == Fmt::I8R) {
+            xr[tt][4 * q + 0] = v.x;
+            xr[tt][4 * q + 1] = v.y;
+            xr[tt][4 * q + 2] = v.z;
+            xr[tt][4 * q + 3] = v.w;
+          } else {
+            // word q of the piece holds elements 8q..8q+7: pairs (8q + j, 8q + j + 4)
+            xr[tt][4 * q + 0] = __byte_perm(v.x, v.z, 0x5410);
+            xr[tt][4 * q + 1] = __byte_perm(v.x, v.z, 0x7632);
+            xr[tt][4 * q + 2] = __byte_perm(v.y, v.w, 0x5410);
+            xr[tt][4 * q + 3] = __byte_perm(v.y, v.w, 0x7632);
+          }
         }
       }
     }
@@ -949,7 +999,6 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
   }  // beg < end
 
   // ---- finish the cut tiles of the cluster ----
-  if (beg >= end) grid_dep_wait();  // (warps with work waited before their first load)
   cluster_sync_all();
   if (close_item >= 0) {
     // contributors: the consecutive warps whose ranges meet the tile's units [t0, t1)
@@ -1026,19 +1075,85 @@ cudaError_t launch_t(const GemvParams& p, int grid, cudaStream_t stream) {
 
 // The factored kernel runs in clusters of kFactCluster CTAs, as many clusters as fit on
 // the GPU at once (one wave), never more than there are items.
+bool env_disabled(const char* name) {  // test knob: NAME=0 turns a path off
+  const char* v = std::getenv(name);
+  return v != nullptr && v[0] == '0';
+}
+template <Fmt F>
+constexpr int kChunkK() { return chunk_k<F>(); }
 constexpr int kFactMinSteps = 2;
 constexpr int kMaxDevicesGemv = 64;
 
+// Shared memory an SM offers blocks (sm_103a), and what the static partial slots of one
+// block of the factored kernel take.
+constexpr size_t kSmemPerSMFact = 228 * 1024;
+constexpr size_t kFactStaticBytes = (size_t)kWarps * 2 * 32 * 4 * sizeof(float);
+
+template <Fmt F, int MT, int kSD, bool kXS>
+cudaError_t launch_fact_t(const GemvParams& p, const FactMaps& maps, uint32_t xstride, size_t smem,
+                          cudaStream_t stream) {
+  // co-resident clusters a device for the last dynamic shared-memory size (0: unknown)
+  static int active[kMaxDevicesGemv] = {0};
+  static size_t active_smem[kMaxDevicesGemv] = {0};
+  static std::atomic<uint64_t> smem_set{0};  // devices whose limit is raised
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevicesGemv) dev = 0;
+  const uint64_t bit = 1ull << dev;
+  if (!(smem_set.load(std::memory_order_acquire) & bit)) {
+    const cudaError_t e = cudaFuncSetAttribute(k_gemv_fact<F, MT, kSD, kXS>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)(kSmemPerSMFact / 2));
+    if (e != cudaSuccess) return e;
+    smem_set.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kFactCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  // programmatic dependent launch: the prologue overlaps the previous kernel's tail; the
+  // kernel waits for it (griddepcontrol.wait) before touching activations or outputs
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (active[dev] == 0 || active_smem[dev] != smem) {
+    cfg.gridDim = dim3(kFactCluster * kNumSMsFallback);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, k_gemv_fact<F, MT, kSD, kXS>, &cfg) != cudaSuccess ||
+        n <= 0) {
+      (void)cudaGetLastError();
+      n = kNumSMsFallback * kBlocksPerSM / kFactCluster;
+    }
+    active[dev] = n;
+    active_smem[dev] = smem;
+  }
+  constexpr int64_t kBatch = 8 * MT;
+  const int64_t row_bytes = (F == Fmt::I8R) ? p.K : p.K / 2;
+  const int64_t items = ((p.N + kRows - 1) / kRows) * ((p.M + kBatch - 1) / kBatch);
+  // at least kFactMinSteps steps a warp on average: fewer, fuller warps beat many idle
+  // ones whose cut tiles would need long reductions
+  const int64_t units = items * (row_bytes / (2 * kChunkBytes));
+  int64_t cap = std::min<int64_t>(active[dev], std::max<int64_t>(1, units / (kFactWarps * kFactMinSteps)));
+  if (const char* env = std::getenv("WQ_GEMV_CLUSTERS")) {  // tuning and test knob
+    const int v = std::atoi(env);
+    if (v >= 1) cap = v;
+  }
+  const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(cap, items));
+  cfg.gridDim = dim3((unsigned)(clusters * kFactCluster));
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, k_gemv_fact<F, MT, kSD, kXS>, p, maps, xstride);
+}
+
+// Ring depth and activation staging: four stages a warp; activations staged in shared
+// memory (4-bit formats, up to 8 rows) when two blocks an SM still fit, with the ring cut
+// to three stages if that is what makes them fit (K = 14336 at one row).
 template <Fmt F, int MT>
 cudaError_t launch_fact(const GemvParams& p, cudaStream_t stream) {
-  static int active[kMaxDevicesGemv] = {0};  // co-resident clusters a device (0: unknown)
-  static std::atomic<bool> smem_set{false};
-  if (!smem_set.load(std::memory_order_acquire)) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        k_gemv_fact<F, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kFactSmemBytes);
-    if (e != cudaSuccess) return e;
-    smem_set.store(true, std::memory_order_release);
-  }
   // tensor maps of codes, scales and zero points
   FactMaps maps;
   const int64_t row_bytes = (F == Fmt::I8R) ? p.K : p.K / 2;
@@ -1060,46 +1175,20 @@ cudaError_t launch_fact(const GemvParams& p, cudaStream_t stream) {
       return cudaErrorInvalidValue;
     maps.z = maps.s;  // unused
   }
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevicesGemv) dev = 0;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kFactCluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  // programmatic dependent launch: the prologue overlaps the previous kernel's tail; the
-  // kernel waits for it (griddepcontrol.wait) before touching global memory
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kFactSmemBytes;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (active[dev] == 0) {
-    cfg.gridDim = dim3(kFactCluster * kNumSMsFallback);
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, k_gemv_fact<F, MT>, &cfg) != cudaSuccess || n <= 0) {
-      (void)cudaGetLastError();
-      n = kNumSMsFallback * kBlocksPerSM / kFactCluster;
-    }
-    active[dev] = n;
+  const size_t ring4 = 1024 + (size_t)fact_ring_bytes(4), ring3 = 1024 + (size_t)fact_ring_bytes(3);
+  if constexpr (F != Fmt::I8R && MT == 1) {
+    const bool x_ok = !env_disabled("WQ_GEMV_XSMEM") && p.K % kChunkK<F>() == 0 &&
+                      (reinterpret_cast<uintptr_t>(p.x) % 16) == 0;
+    const uint32_t xstride = (uint32_t)(p.M > 1 ? p.K * 2 + kFactXPad : p.K * 2);
+    const size_t xbytes = (size_t)p.M * xstride;
+    // two blocks an SM: (dynamic + static + the 1 KB the driver reserves) twice
+    auto fits = [&](size_t dyn) { return 2 * (dyn + kFactStaticBytes + 1024) <= kSmemPerSMFact; };
+    if (x_ok && fits(ring4 + xbytes))
+      return launch_fact_t<F, MT, 4, true>(p, maps, xstride, ring4 + xbytes, stream);
+    if (x_ok && fits(ring3 + xbytes))
+      return launch_fact_t<F, MT, 3, true>(p, maps, xstride, ring3 + xbytes, stream);
   }
-  constexpr int64_t kBatch = 8 * MT;
-  const int64_t items = ((p.N + kRows - 1) / kRows) * ((p.M + kBatch - 1) / kBatch);
-  // at least kFactMinSteps steps a warp on average: fewer, fuller warps beat many idle
-  // ones whose cut tiles would need long reductions
-  const int64_t units = items * (row_bytes / (2 * kChunkBytes));
-  int64_t cap = std::min<int64_t>(active[dev], std::max<int64_t>(1, units / (kFactWarps * kFactMinSteps)));
-  if (const char* env = std::getenv("WQ_GEMV_CLUSTERS")) {  // tuning and test knob
-    const int v = std::atoi(env);
-    if (v >= 1) cap = v;
-  }
-  const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(cap, items));
-  cfg.gridDim = dim3((unsigned)(clusters * kFactCluster));
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, k_gemv_fact<F, MT>, p, maps);
+  return launch_fact_t<F, MT, 4, false>(p, maps, 0, ring4, stream);
 }
 
 // I4G with a group of at least 128 codes, I4R, I8R: the factored kernel (warp MMA,
