@@ -373,3 +373,29 @@ def test_factored_activation_paths(cuda_device, monkeypatch, xsmem, M, N, K):
     y = run_i4g(d, dev(x, d), dev(packed, d), dev(scale, d), dev(zero, d), None, G)
     yr, ad = oracle.linear_int4_groups(bf16_bits(x), packed, scale, zero, None, N, G)
     assert_within(y, yr, ad, f"xsmem={xsmem} M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("push", ["1", "0"])
+@pytest.mark.parametrize("M,N,K,clusters", [(1, 14336, 4096, None), (1, 4096, 14336, None), (1, 1024, 4096, None),
+                                            (4, 1000, 6144, 5), (12, 700, 4096, None), (1, 256, 2048, 3)])
+def test_factored_cut_tile_fixup(cuda_device, monkeypatch, push, M, N, K, clusters):
+    """Tiles cut between warps are finished either by pushes into the closing warp's
+    shared memory (no cluster-wide barrier) or by the closing warp reading the parked
+    partials after cluster barriers; both match the oracle and are deterministic."""
+    monkeypatch.setenv("WQ_GEMV_PUSH", push)
+    if clusters is not None:
+        monkeypatch.setenv("WQ_GEMV_CLUSTERS", str(clusters))
+    d = cuda_device
+    G = 128
+    packed, scale, zero = make_i4g(N, K, G, seed=N + M)
+    x = synth.normal_bf16((M, K), seed=M + 50)
+    b = synth.normal_bf16((N,), seed=51)
+    args = (dev(x, d), dev(packed, d), dev(scale, d), dev(zero, d), dev(b, d), G)
+    y = run_i4g(d, *args)
+    rows = np.unique(np.concatenate([np.arange(min(N, 64)), np.arange(max(0, N - 64), N),
+                                     np.random.default_rng(5).choice(N, min(N, 256), replace=False)]))
+    yr, ad = oracle.linear_int4_groups(bf16_bits(x), packed[rows], scale[rows], zero[rows], bf16_bits(b)[rows],
+                                       len(rows), G)
+    assert_within(y[:, torch.from_numpy(rows).to(d)], yr, ad, f"push={push} M={M} N={N} K={K}")
+    y2 = run_i4g(d, *args)
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))

@@ -629,6 +629,17 @@ __device__ __forceinline__ void emit_tile(const GemvParams& p, int64_t item, int
 // are in flight while one is computed, independent of the register budget.  Rows past N
 // arrive as zeros (TMA fills out-of-bounds boxes) and are never stored.  Activation rows
 // past M are clamped to the last one (those MMA columns are never stored).
+// kPush: tiles cut between warps are finished without cluster-wide barriers.  Every
+// contributing warp stores its partial D fragment (16 rows x M columns) straight into a
+// receive slot of the closing warp (the one holding the tile's last step) through
+// distributed shared memory and arrives on that warp's mbarrier; only the closing warp
+// waits, then adds the slots in warp order (deterministic) and its own partial last.
+// geo.cmax: receive slots a warp (the most warps any tile of the launch meets).
+struct FactGeom {
+  uint32_t xstride;  // bytes between staged activation rows
+  uint32_t cmax;     // receive slots a warp (push fixup)
+};
+
 struct FactMaps {
   CUtensorMap w;  // codes [N rows, row_bytes], box {128, 16}, 128-byte swizzle
   CUtensorMap s;  // I4G: scales [N, K/G] f32, box {4, 16}; I4R / I8R: scales [N] f32, box {16, 1}
@@ -649,9 +660,10 @@ __host__ __device__ constexpr int fact_ring_bytes(int kSD) {
 // order of the MMA fragments ([row][k / 128][(k / 8) % 4][(k / 32) % 4] 16-byte pieces
 // holding (x0, x4) (x1, x5) (x2, x6) (x3, x7)), so that a lane's B fragments are four
 // 16-byte shared loads a chunk, with no shuffles and no global-memory latency in the loop.
-template <Fmt F, int MT, int kSD, bool kXS>
+template <Fmt F, int MT, int kSD, bool kXS, bool kPush>
 __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
-    k_gemv_fact(const GemvParams p, const __grid_constant__ FactMaps maps, const uint32_t xstride) {
+    k_gemv_fact(const GemvParams p, const __grid_constant__ FactMaps maps, const FactGeom geo) {
+  const uint32_t xstride = geo.xstride;
   static_assert(F == Fmt::I4G || F == Fmt::I4R || F == Fmt::I8R, "affine formats only");
   constexpr int kPiece = piece_k<F>();   // k of a lane's 16 bytes
   constexpr int kChunkK = chunk_k<F>();  // k of a 64-byte chunk
@@ -714,6 +726,9 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
   // bf16x2 (128, 128), derived from a kernel argument so that it stays in a register
   const uint32_t magic = 0x43004300u | (uint32_t)(p.K >> 62);
   int close_item = -1;  // the cut tile this warp finishes after the cluster barrier
+  float ctot[MT][4];    // push fixup: the partial of the tile this warp closes
+#pragma unroll
+  for (int tt = 0; tt < MT; ++tt) ctot[tt][0] = ctot[tt][1] = ctot[tt][2] = ctot[tt][3] = 0.0f;
 
   const int total = beg < end ? (int)(end - beg) : 0;
   // ---- producer side: lane 0 fills stage (u mod kS) with the data of unit beg + u; its
@@ -742,9 +757,37 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
       tma_load_2d(sst + stage * kFactStageS, &maps.s, bar, row0, 0, pol_keep);
     }
   };
+  // push fixup: receive slots [warp][cmax][16 rows][M] f32 and one mbarrier a warp, after
+  // the staged activations
+  uint8_t* const xs = smem + fact_ring_bytes(kS);
+  float* const recv = reinterpret_cast<float*>(
+      xs + (kXS ? (((uint32_t)M * xstride + 15u) & ~15u) : 0u));
+  uint64_t* const recvbar = reinterpret_cast<uint64_t*>(recv + (size_t)kWarps * geo.cmax * 16 * M);
+  // the tile this warp closes in the push fixup: its first segment, cut (the range starts
+  // inside the tile) and ending inside the range; and how many lanes arrive for it
+  uint32_t push_arrivals = 0;
+  if constexpr (kPush) {
+    if (beg < end && beg % spt != 0 && (beg / spt + 1) * spt <= end) {
+      close_item = (int)(beg / spt);
+      const Split sp = split();
+      const uint32_t t0 = (uint32_t)close_item * spt;
+      uint32_t w0 = sp.wc;
+      while (w0 > 0 && sp.bound(w0) > t0) --w0;
+      for (uint32_t w = w0; w < sp.wc; ++w)
+        if (sp.bound(w) < sp.bound(w + 1) && sp.bound(w + 1) > t0) push_arrivals += 32;
+    }
+  }
   if (lane == 0) {
     for (int i = 0; i < kS; ++i) mbar_init(bars + i, 1);
+    if constexpr (kPush) mbar_init(recvbar + warp, push_arrivals > 0 ? push_arrivals : 1u);
     fence_mbar_init();
+  }
+  bool cl_waited = false;  // this warp has passed the cluster barrier's wait
+  if constexpr (kPush) {
+    // every CTA's receive barriers are initialized before any warp of the cluster arrives
+    // on them: arrive now, wait just before the first push (or at the end)
+    __syncwarp();
+    cluster_arrive_release();
   }
   // everything above overlaps the previous kernel (programmatic dependent launch).  Before
   // the wait, only the weights (codes, scales, zero points) may be read, and only when the
@@ -758,7 +801,6 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
   }
   __syncwarp();
 
-  uint8_t* const xs = smem + fact_ring_bytes(kS);
   if constexpr (kXS) {
     // every thread of the block stages activations: eight independent 16-byte loads in
     // flight a thread, then their permuted stores
@@ -974,6 +1016,40 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     if (tile_end || u + 1 == total) {
       if (seg_from_start && tile_end) {
         emit_tile(p, item, tiles, kBatch, tot, g8, cq);
+      } else if (kPush && tile_end) {
+        // this warp closes the tile: keep its own partial until the others' have arrived
+#pragma unroll
+        for (int tt = 0; tt < MT; ++tt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) ctot[tt][i] = tot[tt][i];
+      } else if (kPush) {
+        // a contributor: store the partial into the closing warp's receive slot
+        if (!cl_waited) {
+          cluster_wait_acquire();
+          cl_waited = true;
+        }
+        const Split sp = split();
+        const uint32_t t0 = item * spt, tl = t0 + spt - 1;
+        uint32_t w0 = sp.wc;
+        while (w0 > 0 && sp.bound(w0) > t0) --w0;
+        uint32_t wcl = sp.wc;
+        while (wcl + 1 < (uint32_t)kFactWarps && sp.bound(wcl + 1) <= tl) ++wcl;
+        const uint32_t rank = wcl / kWarps, wl = wcl % kWarps;
+        const uint32_t slot =
+            smem_u32(recv) + ((wl * geo.cmax + (sp.wc - w0)) * 16u * (uint32_t)M) * 4u;
+#pragma unroll
+        for (int tt = 0; tt < MT; ++tt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int col = tt * 8 + 2 * cq + (i & 1), row = g8 + ((i >> 1) << 3);
+            if (col < M)
+              st_shared_cluster_f32(map_shared_rank(slot + (uint32_t)(row * M + col) * 4u, rank),
+                                    tot[tt][i]);
+          }
+        // every lane arrives (release, cluster scope) after its own stores: one arrival a
+        // lane orders exactly that lane's stores, with no fence (measured cheaper than a
+        // cluster fence a lane and one arrival a warp)
+        mbar_arrive_remote(map_shared_rank(smem_u32(recvbar + wl), rank));
       } else {
         // a cut tile: park the partial; the warp holding the tile's last step (this
         // one, if the tile ends here) adds the partials up later
@@ -999,6 +1075,41 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
   }  // beg < end
 
   // ---- finish the cut tiles of the cluster ----
+  if constexpr (kPush) {
+    if (!cl_waited) cluster_wait_acquire();  // every thread passes the barrier once
+    if (close_item >= 0) {
+      // contributors w0 .. wc - 1 (in warp order; empty ranges add nothing), then this warp
+      if (!mbar_wait_cluster(recvbar + warp, 0)) {
+        set_dev_status(p.dev_status, WQ_DEV_TIMEOUT);
+        return;
+      }
+      const Split sp = split();
+      const uint32_t t0 = (uint32_t)close_item * spt;
+      uint32_t w0 = sp.wc;
+      while (w0 > 0 && sp.bound(w0) > t0) --w0;
+      float tot[MT][4];
+#pragma unroll
+      for (int tt = 0; tt < MT; ++tt) tot[tt][0] = tot[tt][1] = tot[tt][2] = tot[tt][3] = 0.0f;
+      const float* base = recv + (size_t)warp * geo.cmax * 16 * M;
+      for (uint32_t w = w0; w < sp.wc; ++w) {
+        if (!(sp.bound(w) < sp.bound(w + 1) && sp.bound(w + 1) > t0)) continue;
+        const float* sl = base + (size_t)(w - w0) * 16 * M;
+#pragma unroll
+        for (int tt = 0; tt < MT; ++tt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int col = tt * 8 + 2 * cq + (i & 1), row = g8 + ((i >> 1) << 3);
+            if (col < M) tot[tt][i] += sl[row * M + col];
+          }
+      }
+#pragma unroll
+      for (int tt = 0; tt < MT; ++tt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) tot[tt][i] += ctot[tt][i];
+      emit_tile(p, close_item, tiles, kBatch, tot, g8, cq);
+    }
+    return;
+  }
   cluster_sync_all();
   if (close_item >= 0) {
     // contributors: the consecutive warps whose ranges meet the tile's units [t0, t1)
@@ -1089,9 +1200,9 @@ constexpr int kMaxDevicesGemv = 64;
 constexpr size_t kSmemPerSMFact = 228 * 1024;
 constexpr size_t kFactStaticBytes = (size_t)kWarps * 2 * 32 * 4 * sizeof(float);
 
-template <Fmt F, int MT, int kSD, bool kXS>
-cudaError_t launch_fact_t(const GemvParams& p, const FactMaps& maps, uint32_t xstride, size_t smem,
-                          cudaStream_t stream) {
+template <Fmt F, int MT, int kSD, bool kXS, bool kPush>
+cudaError_t launch_fact_t(const GemvParams& p, const FactMaps& maps, const FactGeom& geo,
+                          size_t smem, int64_t clusters, cudaStream_t stream) {
   // co-resident clusters a device for the last dynamic shared-memory size (0: unknown)
   static int active[kMaxDevicesGemv] = {0};
   static size_t active_smem[kMaxDevicesGemv] = {0};
@@ -1100,7 +1211,7 @@ cudaError_t launch_fact_t(const GemvParams& p, const FactMaps& maps, uint32_t xs
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevicesGemv) dev = 0;
   const uint64_t bit = 1ull << dev;
   if (!(smem_set.load(std::memory_order_acquire) & bit)) {
-    const cudaError_t e = cudaFuncSetAttribute(k_gemv_fact<F, MT, kSD, kXS>,
+    const cudaError_t e = cudaFuncSetAttribute(k_gemv_fact<F, MT, kSD, kXS, kPush>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                (int)(kSmemPerSMFact / 2));
     if (e != cudaSuccess) return e;
@@ -1124,7 +1235,7 @@ cudaError_t launch_fact_t(const GemvParams& p, const FactMaps& maps, uint32_t xs
   if (active[dev] == 0 || active_smem[dev] != smem) {
     cfg.gridDim = dim3(kFactCluster * kNumSMsFallback);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, k_gemv_fact<F, MT, kSD, kXS>, &cfg) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveClusters(&n, k_gemv_fact<F, MT, kSD, kXS, kPush>, &cfg) != cudaSuccess ||
         n <= 0) {
       (void)cudaGetLastError();
       n = kNumSMsFallback * kBlocksPerSM / kFactCluster;
@@ -1132,21 +1243,10 @@ cudaError_t launch_fact_t(const GemvParams& p, const FactMaps& maps, uint32_t xs
     active[dev] = n;
     active_smem[dev] = smem;
   }
-  constexpr int64_t kBatch = 8 * MT;
-  const int64_t row_bytes = (F == Fmt::I8R) ? p.K : p.K / 2;
-  const int64_t items = ((p.N + kRows - 1) / kRows) * ((p.M + kBatch - 1) / kBatch);
-  // at least kFactMinSteps steps a warp on average: fewer, fuller warps beat many idle
-  // ones whose cut tiles would need long reductions
-  const int64_t units = items * (row_bytes / (2 * kChunkBytes));
-  int64_t cap = std::min<int64_t>(active[dev], std::max<int64_t>(1, units / (kFactWarps * kFactMinSteps)));
-  if (const char* env = std::getenv("WQ_GEMV_CLUSTERS")) {  // tuning and test knob
-    const int v = std::atoi(env);
-    if (v >= 1) cap = v;
-  }
-  const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(cap, items));
-  cfg.gridDim = dim3((unsigned)(clusters * kFactCluster));
+  if (clusters > active[dev]) clusters = active[dev];  // one wave (the caller sized it)
+  cfg.gridDim = dim3((unsigned)(std::max<int64_t>(1, clusters) * kFactCluster));
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, k_gemv_fact<F, MT, kSD, kXS>, p, maps, xstride);
+  return cudaLaunchKernelEx(&cfg, k_gemv_fact<F, MT, kSD, kXS, kPush>, p, maps, geo);
 }
 
 // Ring depth and activation staging: four stages a warp; activations staged in shared
@@ -1175,20 +1275,66 @@ cudaError_t launch_fact(const GemvParams& p, cudaStream_t stream) {
       return cudaErrorInvalidValue;
     maps.z = maps.s;  // unused
   }
+  // clusters: as many as are co-resident (a fixed 2 blocks an SM on 152 SMs bounds it; the
+  // launch clamps to the measured figure), at least kFactMinSteps steps a warp on average
+  // (fewer, fuller warps beat many idle ones), never more than there are items
+  constexpr int64_t kBatch = 8 * MT;
+  const int64_t items = ((p.N + kRows - 1) / kRows) * ((p.M + kBatch - 1) / kBatch);
+  const int64_t spt = row_bytes / (2 * kChunkBytes);
+  int64_t cap = std::min<int64_t>(kNumSMsFallback * kBlocksPerSM / kFactCluster,
+                                  std::max<int64_t>(1, items * spt / (kFactWarps * kFactMinSteps)));
+  if (const char* env = std::getenv("WQ_GEMV_CLUSTERS")) {  // tuning and test knob
+    const int v = std::atoi(env);
+    if (v >= 1) cap = v;
+  }
+  const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(cap, items));
+  // push fixup: receive slots a warp = the most warps any cut tile meets, from the same
+  // split as the kernel (cluster c takes q or q + 1 items; warp w of a cluster starts at
+  // unit (w * U) >> 6)
+  uint32_t cmax = 1;
+  {
+    const int64_t q = items / clusters;
+    for (int64_t icnt = std::max<int64_t>(q, 1); icnt <= q + 1; ++icnt) {
+      const uint64_t U = (uint64_t)(icnt * spt);
+      auto bound = [&](uint64_t w) { return (w * U) >> 6; };
+      auto owner = [&](uint64_t u) {
+        uint64_t w = 0;
+        while (w + 1 < (uint64_t)kFactWarps && bound(w + 1) <= u) ++w;
+        return w;
+      };
+      for (int64_t t = 0; t < icnt; ++t) {
+        const uint64_t w0 = owner((uint64_t)(t * spt)), w1 = owner((uint64_t)(t * spt + spt - 1));
+        cmax = std::max<uint32_t>(cmax, (uint32_t)(w1 - w0 + 1));
+      }
+    }
+  }
   const size_t ring4 = 1024 + (size_t)fact_ring_bytes(4), ring3 = 1024 + (size_t)fact_ring_bytes(3);
+  const size_t recv = (size_t)kWarps * cmax * 16 * (size_t)p.M * 4 + kWarps * 8;
+  // the push fixup pays where few warps share a tile (the closing warp waits for each in
+  // turn); with many (long rows or small N) the cluster barriers do better, as measured
+  const char* push_env = std::getenv("WQ_GEMV_PUSH");  // test knob: 1 forces it, 0 disables it
+  const bool push_ok = push_env ? (push_env[0] == '1' && cmax <= 32) : (cmax <= 4);
+  // two blocks an SM: (dynamic + static + the 1 KB the driver reserves) twice
+  auto fits = [&](size_t dyn) { return 2 * (dyn + kFactStaticBytes + 1024) <= kSmemPerSMFact; };
   if constexpr (F != Fmt::I8R && MT == 1) {
     const bool x_ok = !env_disabled("WQ_GEMV_XSMEM") && p.K % kChunkK<F>() == 0 &&
                       (reinterpret_cast<uintptr_t>(p.x) % 16) == 0;
     const uint32_t xstride = (uint32_t)(p.M > 1 ? p.K * 2 + kFactXPad : p.K * 2);
-    const size_t xbytes = (size_t)p.M * xstride;
-    // two blocks an SM: (dynamic + static + the 1 KB the driver reserves) twice
-    auto fits = [&](size_t dyn) { return 2 * (dyn + kFactStaticBytes + 1024) <= kSmemPerSMFact; };
+    const size_t xbytes = ((size_t)p.M * xstride + 15) & ~size_t(15);
+    const FactGeom geo{xstride, cmax};
+    if (x_ok && push_ok && fits(ring4 + xbytes + recv))
+      return launch_fact_t<F, MT, 4, true, true>(p, maps, geo, ring4 + xbytes + recv, clusters, stream);
+    if (x_ok && push_ok && fits(ring3 + xbytes + recv))
+      return launch_fact_t<F, MT, 3, true, true>(p, maps, geo, ring3 + xbytes + recv, clusters, stream);
     if (x_ok && fits(ring4 + xbytes))
-      return launch_fact_t<F, MT, 4, true>(p, maps, xstride, ring4 + xbytes, stream);
+      return launch_fact_t<F, MT, 4, true, false>(p, maps, geo, ring4 + xbytes, clusters, stream);
     if (x_ok && fits(ring3 + xbytes))
-      return launch_fact_t<F, MT, 3, true>(p, maps, xstride, ring3 + xbytes, stream);
+      return launch_fact_t<F, MT, 3, true, false>(p, maps, geo, ring3 + xbytes, clusters, stream);
   }
-  return launch_fact_t<F, MT, 4, false>(p, maps, 0, ring4, stream);
+  const FactGeom geo{0, cmax};
+  if (push_ok && fits(ring4 + recv))
+    return launch_fact_t<F, MT, 4, false, true>(p, maps, geo, ring4 + recv, clusters, stream);
+  return launch_fact_t<F, MT, 4, false, false>(p, maps, geo, ring4, clusters, stream);
 }
 
 // I4G with a group of at least 128 codes, I4R, I8R: the factored kernel (warp MMA,
