@@ -375,14 +375,52 @@ def test_factored_activation_paths(cuda_device, monkeypatch, xsmem, M, N, K):
     assert_within(y, yr, ad, f"xsmem={xsmem} M={M} N={N} K={K}")
 
 
-@pytest.mark.parametrize("push", ["1", "0"])
+@pytest.mark.parametrize("fmt", ["groups", "rows"])
+@pytest.mark.parametrize("M", [1, 3, 8])
+def test_decode_offset_activations_full_range_zero_points(cuda_device, M, fmt):
+    """Activations with a large common offset (mean 6, so that the sums of x_k * (q_k - z)
+    are small differences of large terms) and zero points over the whole byte range
+    (signed per-row codes: the fixed offset 8) match the oracle, column by column (M = 3
+    leaves MMA columns past M)."""
+    d = cuda_device
+    N, K = 600, 4096
+    x = (synth.normal_bf16((M, K), seed=M + 71).float() + 6.0).to(torch.bfloat16)
+    if fmt == "groups":
+        G = 128
+        rng = np.random.default_rng(M + 70)
+        packed = rng.integers(0, 256, (N, K // 2)).astype(np.uint8)
+        scale = (rng.random((N, K // G)) * 0.018 + 0.002).astype(np.float32)
+        zero = rng.integers(0, 256, (N, K // G)).astype(np.uint8)
+        y = run_i4g(d, dev(x, d), dev(packed, d), dev(scale, d), dev(zero, d), None, G)
+        yr, ad = oracle.linear_int4_groups(bf16_bits(x), packed, scale, zero, None, N, G)
+    else:
+        w = synth.weight_f32(N, K, seed=N + 72)
+        q, s, _ = oracle.quantize_sym(w.numpy(), K, 4)
+        _, p = oracle.pack_int4(q, False)
+        ws = wq.alloc_workspace(wq.wq_linear_rows_workspace(M, N, K, 4), d)
+        buf, y = guarded((M, N), torch.bfloat16, d)
+        wq.wq_linear_int4_rows(dev(x, d), dev(p.view(np.int8), d), dev(s[:, 0].copy(), d), None, y=y, workspace=ws)
+        torch.cuda.synchronize()
+        assert guards_intact(buf)
+        yr, ad = oracle.linear_int4_rows(bf16_bits(x), p, s[:, 0].copy())
+    assert_within(y, yr, ad, f"offset activations {fmt} M={M}")
+
+
+@pytest.mark.parametrize("mode", ["push", "barrier", "default"])
 @pytest.mark.parametrize("M,N,K,clusters", [(1, 14336, 4096, None), (1, 4096, 14336, None), (1, 1024, 4096, None),
-                                            (4, 1000, 6144, 5), (12, 700, 4096, None), (1, 256, 2048, 3)])
-def test_factored_cut_tile_fixup(cuda_device, monkeypatch, push, M, N, K, clusters):
-    """Tiles cut between warps are finished either by pushes into the closing warp's
-    shared memory (no cluster-wide barrier) or by the closing warp reading the parked
-    partials after cluster barriers; both match the oracle and are deterministic."""
-    monkeypatch.setenv("WQ_GEMV_PUSH", push)
+                                            (1, 4096, 4096, None), (4, 1000, 6144, 5), (12, 700, 4096, None),
+                                            (1, 256, 2048, 3)])
+def test_factored_cut_tile_fixup(cuda_device, monkeypatch, mode, M, N, K, clusters):
+    """Tiles cut between warps are finished by pushes into the closing warp's shared
+    memory (no cluster-wide barrier), by the closing warp reading the parked partials
+    after cluster barriers, or (the default where every cut tile lies inside one block,
+    e.g. 4096 x 4096 and 1024 x 4096 at M = 1) after a block barrier; all match the oracle
+    and are deterministic."""
+    if mode == "push":
+        monkeypatch.setenv("WQ_GEMV_PUSH", "1")
+    elif mode == "barrier":
+        monkeypatch.setenv("WQ_GEMV_PUSH", "0")
+        monkeypatch.setenv("WQ_GEMV_LOCAL", "0")
     if clusters is not None:
         monkeypatch.setenv("WQ_GEMV_CLUSTERS", str(clusters))
     d = cuda_device
@@ -396,6 +434,6 @@ def test_factored_cut_tile_fixup(cuda_device, monkeypatch, push, M, N, K, cluste
                                      np.random.default_rng(5).choice(N, min(N, 256), replace=False)]))
     yr, ad = oracle.linear_int4_groups(bf16_bits(x), packed[rows], scale[rows], zero[rows], bf16_bits(b)[rows],
                                        len(rows), G)
-    assert_within(y[:, torch.from_numpy(rows).to(d)], yr, ad, f"push={push} M={M} N={N} K={K}")
+    assert_within(y[:, torch.from_numpy(rows).to(d)], yr, ad, f"{mode} M={M} N={N} K={K}")
     y2 = run_i4g(d, *args)
     assert torch.equal(y.view(torch.int16), y2.view(torch.int16))

@@ -226,7 +226,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const int t = threadIdx.x - 64;  // weight row of the tile owned by this thread
     const int64_t n = imin64(n0 + t, N - 1);
     const int gshift = __ffs(p.group) - 1;
-    const int64_t gpr = K >> gshift;
+    const uint32_t gpr = (uint32_t)(K >> gshift);  // groups a row (K < 2^31)
+    const float* const srow = p.scale + n * (int64_t)gpr;
+    const uint8_t* const zrow = p.zero + n * (int64_t)gpr;
     const bool two_groups = (p.group < kBK);  // group 32: two groups a k step
 
     struct Meta {
@@ -236,13 +238,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     auto load_meta = [&](int kb) -> Meta {
       Meta m{1.0f, 1.0f, 0u};
       if (kb >= nk) return m;
-      const int64_t g0 = imin64(((int64_t)(kb0 + kb) * kBK) >> gshift, gpr - 1);
-      const int64_t g1 = imin64(g0 + 1, gpr - 1);
-      m.s0 = __ldg(&p.scale[n * gpr + g0]);
-      m.z = __ldg(&p.zero[n * gpr + g0]);
+      const uint32_t g0 = min(((uint32_t)(kb0 + kb) * (uint32_t)kBK) >> gshift, gpr - 1);
+      m.s0 = __ldg(srow + g0);
+      m.z = __ldg(zrow + g0);
       if (two_groups) {
-        m.s1 = __ldg(&p.scale[n * gpr + g1]);
-        m.z |= (uint32_t)__ldg(&p.zero[n * gpr + g1]) << 8;
+        const uint32_t g1 = min(g0 + 1, gpr - 1);
+        m.s1 = __ldg(srow + g1);
+        m.z |= (uint32_t)__ldg(zrow + g1) << 8;
       }
       return m;
     };
@@ -250,37 +252,46 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 
     const uint32_t prow = (uint32_t)t * 32;  // packed row, 32-byte swizzle
     const uint32_t pswz = (uint32_t)((t >> 2) & 1);
-    const uint32_t brow = (uint32_t)t * 128;  // dequantized row, 128-byte swizzle
-    const uint32_t bswz = (uint32_t)(t & 7);
+    // this thread's eight 16-byte pieces of its dequantized row: piece w at w ^ (row mod 8)
+    // (128-byte swizzle), offsets inside a stage
+    uint32_t boff[8];
+#pragma unroll
+    for (int w = 0; w < 8; ++w) boff[w] = (uint32_t)t * 128 + (((uint32_t)w ^ (uint32_t)(t & 7)) << 4);
+    const uint32_t pa0 = prow + (pswz << 4), pa1 = prow + ((1u ^ pswz) << 4);
+
+    // one k step: the packed row from the stage, dequantized, into the MMA's layout
+    auto dequant_step = [&](int s, const Nib8Consts& k0, const Nib8Consts& k1) {
+      const uint32_t pbase = smem_u32(stage_p(s));
+      const uint4 c0 = ld_shared_v4(pbase + pa0);
+      const uint4 c1 = ld_shared_v4(pbase + pa1);
+      const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+      const uint32_t bbase = smem_u32(stage_b(s));
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        uint32_t o[4];
+        dequant_nib8(words[w], (w < 4) ? k0 : k1, o);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(bbase + boff[w]), "r"(o[0]),
+                     "r"(o[1]), "r"(o[2]), "r"(o[3])
+                     : "memory");
+      }
+    };
 
     for (int kb = 0; kb < nk; ++kb) {
       const int s = kb % kStagesTc;
       const Meta m = mq0;
       mq0 = mq1;
       mq1 = load_meta(kb + 2);
-      const Nib8Consts k0 = make_nib8_consts_u(m.s0, m.z & 0xFFu);
-      Nib8Consts k1 = k0;
-      if (two_groups) k1 = make_nib8_consts_u(m.s1, (m.z >> 8) & 0xFFu);
       if (*reinterpret_cast<volatile int*>(&sh->abort)) break;
       if (!mbar_wait(&sh->full_tma[s], (kb / kStagesTc) & 1)) {
         set_dev_status(p.dev_status, WQ_DEV_TIMEOUT);
         atomicExch(&sh->abort, 1);
         break;
       }
-      const uint32_t pbase = smem_u32(stage_p(s)) + prow;
-      const uint4 c0 = ld_shared_v4(pbase + ((0u ^ pswz) << 4));
-      const uint4 c1 = ld_shared_v4(pbase + ((1u ^ pswz) << 4));
-      const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-      const uint32_t bbase = smem_u32(stage_b(s)) + brow;
-#pragma unroll
-      for (int w = 0; w < 8; ++w) {
-        uint32_t o[4];
-        dequant_nib8(words[w], (w < 4) ? k0 : k1, o);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                         bbase + (((uint32_t)w ^ bswz) << 4)),
-                     "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
-                     : "memory");
-      }
+      const Nib8Consts k0 = make_nib8_consts_u(m.s0, m.z & 0xFFu);
+      if (two_groups)
+        dequant_step(s, k0, make_nib8_consts_u(m.s1, (m.z >> 8) & 0xFFu));
+      else
+        dequant_step(s, k0, k0);
       fence_async_shared();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh->full_b[s]);
@@ -312,7 +323,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
                             __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
         } else {
-          for (int i = 0; i < 32 && nb + i < N; ++i) dst[i] = __uint_as_float(r[i]);
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (nb + i < N) dst[i] = __uint_as_float(r[i]);
         }
       } else if (m < M && nb < N) {
         float v[32];
@@ -333,7 +346,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             *reinterpret_cast<uint4*>(dst + 8 * i) = o;
           }
         } else {
-          for (int i = 0; i < 32 && nb + i < N; ++i) dst[i] = __float2bfloat16_rn(v[i]);
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (nb + i < N) dst[i] = __float2bfloat16_rn(v[i]);
         }
       }
     }

@@ -1275,13 +1275,17 @@ cudaError_t launch_fact(const GemvParams& p, cudaStream_t stream) {
       return cudaErrorInvalidValue;
     maps.z = maps.s;  // unused
   }
-  // clusters: as many as are co-resident (a fixed 2 blocks an SM on 152 SMs bounds it; the
-  // launch clamps to the measured figure), at least kFactMinSteps steps a warp on average
-  // (fewer, fuller warps beat many idle ones), never more than there are items
+  // clusters: at most nine tenths of those co-resident (a fixed 2 blocks an SM on 152 SMs
+  // bounds it; the launch clamps to the measured figure), at least kFactMinSteps steps a
+  // warp on average (fewer, fuller warps beat many idle ones), never more than there are
+  // items
   constexpr int64_t kBatch = 8 * MT;
   const int64_t items = ((p.N + kRows - 1) / kRows) * ((p.M + kBatch - 1) / kBatch);
   const int64_t spt = row_bytes / (2 * kChunkBytes);
-  int64_t cap = std::min<int64_t>(kNumSMsFallback * kBlocksPerSM / kFactCluster,
+  // Nine tenths of the clusters two blocks an SM would hold: measured on GB300, 34 clusters
+  // of 8 beat 36 to 38 by 4 to 10 % on the 14336 x 4096 and 4096 x 14336 layers (with 36
+  // or more, the last clusters of a launch start late).
+  int64_t cap = std::min<int64_t>(kNumSMsFallback * kBlocksPerSM * 9 / (10 * kFactCluster),
                                   std::max<int64_t>(1, items * spt / (kFactWarps * kFactMinSteps)));
   if (const char* env = std::getenv("WQ_GEMV_CLUSTERS")) {  // tuning and test knob
     const int v = std::atoi(env);
