@@ -411,16 +411,14 @@ def test_decode_offset_activations_full_range_zero_points(cuda_device, M, fmt):
                                             (1, 4096, 4096, None), (4, 1000, 6144, 5), (12, 700, 4096, None),
                                             (1, 256, 2048, 3)])
 def test_factored_cut_tile_fixup(cuda_device, monkeypatch, mode, M, N, K, clusters):
-    """Tiles cut between warps are finished by pushes into the closing warp's shared
-    memory (no cluster-wide barrier), by the closing warp reading the parked partials
-    after cluster barriers, or (the default where every cut tile lies inside one block,
-    e.g. 4096 x 4096 and 1024 x 4096 at M = 1) after a block barrier; all match the oracle
-    and are deterministic."""
+    """Tiles cut between warps are finished either by pushes into the closing warp's
+    shared memory (no cluster-wide barrier) or by the closing warp reading the parked
+    partials after cluster barriers (forced each way, and the launch's own choice); all
+    match the oracle and are deterministic."""
     if mode == "push":
         monkeypatch.setenv("WQ_GEMV_PUSH", "1")
     elif mode == "barrier":
         monkeypatch.setenv("WQ_GEMV_PUSH", "0")
-        monkeypatch.setenv("WQ_GEMV_LOCAL", "0")
     if clusters is not None:
         monkeypatch.setenv("WQ_GEMV_CLUSTERS", str(clusters))
     d = cuda_device
