@@ -231,24 +231,42 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const uint8_t* const zrow = p.zero + n * (int64_t)gpr;
     const bool two_groups = (p.group < kBK);  // group 32: two groups a k step
 
-    struct Meta {
-      float s0, s1;
-      uint32_t z;
+    // scales and zero points four groups at a time: one 16-byte and one 4-byte load a
+    // thread when the row's groups are aligned (K / G a multiple of 4), the next four
+    // groups prefetched a window ahead; the dequant constants change only with the group
+    const bool vec_meta = (gpr % 4u == 0) && ((reinterpret_cast<uintptr_t>(p.scale) & 15) == 0) &&
+                          ((reinterpret_cast<uintptr_t>(p.zero) & 3) == 0);
+    struct Win {
+      float4 s;
+      uint32_t z;  // zero points of the four groups, one a byte
     };
-    auto load_meta = [&](int kb) -> Meta {
-      Meta m{1.0f, 1.0f, 0u};
-      if (kb >= nk) return m;
-      const uint32_t g0 = min(((uint32_t)(kb0 + kb) * (uint32_t)kBK) >> gshift, gpr - 1);
-      m.s0 = __ldg(srow + g0);
-      m.z = __ldg(zrow + g0);
-      if (two_groups) {
-        const uint32_t g1 = min(g0 + 1, gpr - 1);
-        m.s1 = __ldg(srow + g1);
-        m.z |= (uint32_t)__ldg(zrow + g1) << 8;
+    auto load_win = [&](uint32_t gb) -> Win {
+      Win w{make_float4(1.0f, 1.0f, 1.0f, 1.0f), 0u};
+      if (vec_meta) {
+        if (gb < gpr) {
+          w.s = __ldg(reinterpret_cast<const float4*>(srow + gb));
+          w.z = __ldg(reinterpret_cast<const unsigned int*>(zrow + gb));
+        }
+      } else {
+        float sv[4] = {1.0f, 1.0f, 1.0f, 1.0f};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (gb + i < gpr) {
+            sv[i] = __ldg(srow + gb + i);
+            w.z |= (uint32_t)__ldg(zrow + gb + i) << (8 * i);
+          }
+        }
+        w.s = make_float4(sv[0], sv[1], sv[2], sv[3]);
       }
-      return m;
+      return w;
     };
-    Meta mq0 = load_meta(0), mq1 = load_meta(1);
+    auto pick = [](const float4& v, uint32_t i) {
+      return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+    };
+    uint32_t gb = (((uint32_t)kb0 * (uint32_t)kBK) >> gshift) & ~3u;
+    Win cur = load_win(gb), nxt = load_win(gb + 4);
+    uint32_t gk = 0xFFFFFFFFu;  // group of the constants below
+    Nib8Consts k0{}, k1{};
 
     const uint32_t prow = (uint32_t)t * 32;  // packed row, 32-byte swizzle
     const uint32_t pswz = (uint32_t)((t >> 2) & 1);
@@ -278,20 +296,26 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 
     for (int kb = 0; kb < nk; ++kb) {
       const int s = kb % kStagesTc;
-      const Meta m = mq0;
-      mq0 = mq1;
-      mq1 = load_meta(kb + 2);
+      // this step's group (a step of 64 codes lies in one group, or two of 32)
+      const uint32_t g0 = ((uint32_t)(kb0 + kb) * (uint32_t)kBK) >> gshift;
+      if ((g0 & ~3u) != gb) {  // warp-uniform: the next window of four groups
+        gb += 4;
+        cur = nxt;
+        nxt = load_win(gb + 4);
+      }
+      if (g0 != gk) {
+        gk = g0;
+        const uint32_t i0 = g0 - gb;
+        k0 = make_nib8_consts_u(pick(cur.s, i0), (cur.z >> (8 * i0)) & 0xFFu);
+        k1 = two_groups ? make_nib8_consts_u(pick(cur.s, i0 + 1), (cur.z >> (8 * i0 + 8)) & 0xFFu) : k0;
+      }
       if (*reinterpret_cast<volatile int*>(&sh->abort)) break;
       if (!mbar_wait(&sh->full_tma[s], (kb / kStagesTc) & 1)) {
         set_dev_status(p.dev_status, WQ_DEV_TIMEOUT);
         atomicExch(&sh->abort, 1);
         break;
       }
-      const Nib8Consts k0 = make_nib8_consts_u(m.s0, m.z & 0xFFu);
-      if (two_groups)
-        dequant_step(s, k0, make_nib8_consts_u(m.s1, (m.z >> 8) & 0xFFu));
-      else
-        dequant_step(s, k0, k0);
+      dequant_step(s, k0, k1);
       fence_async_shared();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh->full_b[s]);
