@@ -623,7 +623,8 @@ def run_gpu(args):
 
 def run_profile_case(args):
     """A few launches of one kernel on one projection, for profiler captures: decode_gate /
-    decode_down (M = 1, workspace on, as timed above) or prefill_gate (M = 2048)."""
+    decode_down (M = 1, workspace on, as timed above), prefill_gate (M = 2048) or
+    mxfp4_gateup (MXFP4 experts, one row routed to 4 of 32)."""
     import torch
 
     import weight_only_quantized_linear_gb300 as wq
@@ -632,6 +633,20 @@ def run_profile_case(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     wq.build()
+    if args.profile_case == "mxfp4_gateup":
+        # MXFP4 experts, shared input: E = 32, gate/up N = 5760, K = 2880, one row, top-4
+        E, N, K, S, R = 32, 5760, 2880, 4, 1
+        blocks, scales = synth.mxfp4_experts(E, N, K, seed=800, device=dev)
+        route = synth.routing_topk(R, E, S, seed=901, device=dev)[0]
+        x = synth.normal_bf16((R, 1, K), seed=11, device="cpu").to(dev)
+        y = torch.empty((R, S, N), dtype=torch.bfloat16, device=dev)
+        wsb = wq.wq_mxfp4_experts_shared_workspace(R, S, E, N, K)
+        ws = wq.alloc_workspace(wsb, dev) if wsb else None
+        for _ in range(3):
+            wq.wq_mxfp4_experts_shared(x, blocks, scales, route, y=y, workspace=ws)
+        torch.cuda.synchronize()
+        print(f"profile case {args.profile_case}: R={R} S={S} E={E} N={N} K={K}, 3 launches")
+        return 0
     kind, proj = args.profile_case.split("_")
     N, K = synth.LLAMA_PROJ[proj]
     M = 1 if kind == "decode" else PREFILL_M
@@ -662,7 +677,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
-    ap.add_argument("--profile-case", choices=["decode_gate", "decode_down", "prefill_gate"],
+    ap.add_argument("--profile-case", choices=["decode_gate", "decode_down", "prefill_gate", "mxfp4_gateup"],
                     help="run three launches of one kernel (for profiler captures) and exit")
     args = ap.parse_args()
     if args.impl == "reference":

@@ -50,7 +50,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 
 int run_gemv(Fmt f, GemvParams p, void* workspace, size_t ws_bytes, cudaStream_t stream) {
-  GemvPlan pl = plan_gemv(f, p.M, p.N, p.K, num_sms_current());
+  const int64_t batches = (f == Fmt::MXFP4) ? std::min<int64_t>(p.M * p.S, p.E) : 1;
+  GemvPlan pl = plan_gemv(f, p.M, p.N, p.K, num_sms_current(), batches);
   if (pl.stream_k) {
     if (workspace == nullptr || ws_bytes == 0) {
       pl.stream_k = false;  // whole tiles a warp: correct, less evenly balanced

@@ -1365,12 +1365,13 @@ std::atomic<int> g_static_weights{0};
 void set_static_weights(int on) { g_static_weights.store(on ? 1 : 0, std::memory_order_relaxed); }
 int static_weights() { return g_static_weights.load(std::memory_order_relaxed); }
 
-GemvPlan plan_gemv(Fmt f, int64_t M, int64_t N, int64_t K, int num_sms) {
+GemvPlan plan_gemv(Fmt f, int64_t M, int64_t N, int64_t K, int num_sms, int64_t batches) {
   GemvPlan pl;
   const int ck = (f == Fmt::I8R) ? 64 : 128;
   pl.spt = (int)((K + ck - 1) / ck);  // chunks a tile
   pl.tiles = (int)((N + kRows - 1) / kRows);
-  const int64_t work = (int64_t)pl.tiles * pl.spt;
+  // MXFP4: every tile is streamed once for each routed-expert batch
+  const int64_t work = (int64_t)pl.tiles * pl.spt * std::max<int64_t>(1, batches);
   int64_t blocks = (int64_t)num_sms * kBlocksPerSM;
   if (const char* env = std::getenv("WQ_GEMV_BLOCKS")) {  // tuning knob
     const int v = std::atoi(env);

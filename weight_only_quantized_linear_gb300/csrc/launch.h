@@ -46,7 +46,9 @@ struct GemvPlan {
 // calls) rounded up to 256 bytes, then the f32 partial tiles [warps, 2, M, 16].
 inline size_t ws_counter_bytes(int tiles) { return ((size_t)tiles * 4 + 255) & ~size_t(255); }
 
-GemvPlan plan_gemv(Fmt f, int64_t M, int64_t N, int64_t K, int num_sms);
+// batches: MXFP4 routed-expert batches the launch streams each tile for (an estimate:
+// min(R * S, E)); 1 for the other formats.
+GemvPlan plan_gemv(Fmt f, int64_t M, int64_t N, int64_t K, int num_sms, int64_t batches = 1);
 cudaError_t launch_gemv(Fmt f, GemvParams p, const GemvPlan& plan, cudaStream_t stream);
 // Weights declared immutable by the caller (wq_set_static_weights): decode kernels may
 // start reading them before the previous kernel of the stream has completed.
