@@ -623,7 +623,7 @@ def run_gpu(args):
 
 def run_profile_case(args):
     """A few launches of one kernel on one projection, for profiler captures: decode_gate /
-    decode_down (M = 1, workspace on, as timed above), prefill_gate (M = 2048) or
+    decode_down (M = 1, workspace on, as timed above), prefill_gate / prefill_down (M = 2048) or
     mxfp4_gateup (MXFP4 experts, one row routed to 4 of 32)."""
     import torch
 
@@ -677,7 +677,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
-    ap.add_argument("--profile-case", choices=["decode_gate", "decode_down", "prefill_gate", "mxfp4_gateup"],
+    ap.add_argument("--profile-case", choices=["decode_gate", "decode_down", "prefill_gate", "prefill_down", "mxfp4_gateup"],
                     help="run three launches of one kernel (for profiler captures) and exit")
     args = ap.parse_args()
     if args.impl == "reference":
