@@ -251,6 +251,25 @@ def mxfp4_experts_shared(x, blocks, scales, experts, n: int, n0: int = 0, n1: in
     return y, a, int(bad)
 
 
+def mxfp4_combine_experts(x, blocks, scales, experts, weights, n: int):
+    """mxfp4_combine_experts(x, blocks, scales, experts, weights) ("Quantization" (Linnet
+    docs), format table: std.nn.moe::combine_experts with MXFP4 experts).  The page gives
+    only the name and the arguments; the reading taken: each row's routed slots share the
+    row's input, as in mxfp4_experts_shared, and the row's output is the weighted sum of
+    its slots' outputs,
+        y[r, n] = sum_s weights[r, s] * sum_k x[r, k] * W-hat[experts[r, s], n, k],
+    a slot whose expert index lies outside [0, E) adding nothing.
+
+    x bf16 bits [R, K]; weights f32 [R, S].  Returns (y f64 [R, N], absdot [R, N] =
+    sum_s |weights[r, s]| * sum_k |x w|, bad_slots).
+    """
+    w = _c(weights, np.float32).astype(np.float64)
+    ys, a, bad = mxfp4_experts_shared(x, blocks, scales, experts, n)
+    y = np.einsum("rs,rsn->rn", w, ys)
+    absdot = np.einsum("rs,rsn->rn", np.abs(w), a)
+    return y, absdot, bad
+
+
 def bf16_from_f32(v: float) -> int:
     return int(_load().orc_bf16_from_f32(float(v)))
 

@@ -331,6 +331,43 @@ def test_mxfp4_experts_shared_brute_force():
                 assert np.allclose(y[rr, ss], wdq[ex] @ xf[rr], rtol=0, atol=1e-12)
 
 
+def test_mxfp4_combine_experts_reduces_to_single_slots():
+    """mxfp4_combine_experts (a reading: the weighted sum of the row's slot outputs) against
+    what it must reduce to: one-hot weights pick exactly one slot of mxfp4_experts_shared;
+    a row routed S times to one expert with weights summing to one gives that expert's
+    product (checked against the separately written dequantizer and a plain matmul); an
+    out-of-range slot adds nothing whatever its weight."""
+    rng = np.random.default_rng(21)
+    r, e, n, k, s = 3, 6, 9, 96, 4
+    x = _rand_bf16(rng, (r, k))
+    blocks = rng.integers(0, 256, (e, n, k // 32, 16)).astype(np.uint8)
+    scales = rng.integers(118, 125, (e, n, k // 32)).astype(np.uint8)
+    experts = np.array([[0, 3, 5, 1], [2, 2, 2, 2], [4, 7, 1, 0]], np.int32)  # 7: out of range
+    ys, _, _ = oracle.mxfp4_experts_shared(x, blocks, scales, experts, n)
+    wdq = bf16_bits_to_f64(oracle.dequant_mxfp4(blocks, scales, e, n, k))
+    xf = bf16_bits_to_f64(x)
+    # one-hot weights: slot j of each row (rows of different j: a transposed index fails)
+    pick = np.array([2, 0, 3])
+    onehot = np.zeros((r, s), np.float32)
+    onehot[np.arange(r), pick] = 1.0
+    y1, a1, bad = oracle.mxfp4_combine_experts(x, blocks, scales, experts, onehot, n)
+    assert bad == 1
+    for rr in range(r):
+        assert np.array_equal(y1[rr], ys[rr, pick[rr]])
+    # softmax weights (sum 1) on a row routed four times to expert 2
+    logits = rng.standard_normal((r, s))
+    wsm = (np.exp(logits) / np.exp(logits).sum(axis=1, keepdims=True)).astype(np.float32)
+    y2, a2, _ = oracle.mxfp4_combine_experts(x, blocks, scales, experts, wsm, n)
+    ref = wdq[2] @ xf[1] * float(wsm[1].astype(np.float64).sum())
+    assert np.allclose(y2[1], ref, rtol=1e-12, atol=1e-12)
+    assert (a2[1] > 0).all() and (a2[1] >= np.abs(y2[1]) - 1e-12).all()
+    # the out-of-range slot (row 2, slot 1) carries weight but adds nothing
+    w3 = np.zeros((r, s), np.float32)
+    w3[2, 1] = 5.0
+    y3, a3, _ = oracle.mxfp4_combine_experts(x, blocks, scales, experts, w3, n)
+    assert (y3 == 0).all() and (a3 == 0).all()
+
+
 def test_quantization_error_budget():
     """Sanity (not parity): the quantized layer's output stays within the error budget
     of the quantization step (Delta = s/2 plus the bf16 rounding of W-hat) plus f64
