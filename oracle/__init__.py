@@ -203,6 +203,24 @@ def linear_int4_groups(x, packed, scale, zero, bias, n: int, group: int):
     return y, a
 
 
+def linear_int4_groups_ordered(x, order, packed, scale, zero, bias, n: int, group: int):
+    """Int4GroupLinear with an activation order ("Quantization" (Linnet docs), format table
+    "optional order: [In; i32]", and "Quantizing a checkpoint": a GPTQ checkpoint in
+    activation order "gets an order and gathers its inputs first").  Stored column j of
+    the weights multiplies input order[j]:  y = x[:, order] . W-hat^T + bias.
+
+    Every entry of order must lie in [0, K) (ValueError otherwise).  Returns (y, absdot)
+    as linear_int4_groups.
+    """
+    x = _c(x, np.uint16)
+    order = np.asarray(order)
+    if order.ndim != 1 or order.shape[0] != x.shape[1]:
+        raise ValueError("order must have one entry per input")
+    if (order < 0).any() or (order >= x.shape[1]).any():
+        raise ValueError("order entries must lie in [0, K)")
+    return linear_int4_groups(x[:, order.astype(np.int64)], packed, scale, zero, bias, n, group)
+
+
 def linear_int8_rows(x, q, scale, bias=None):
     x = _c(x, np.uint16)
     m, k = x.shape
@@ -249,6 +267,19 @@ def mxfp4_experts_shared(x, blocks, scales, experts, n: int, n0: int = 0, n1: in
     bad = _load().orc_mxfp4_experts_shared(_ptr(x), r, k, _ptr(blocks), _ptr(scales), e, n,
                                            _ptr(experts), s, n0, n1, _ptr(y), _ptr(a))
     return y, a, int(bad)
+
+
+def mxfp4_experts(x, blocks, scales, experts, n: int):
+    """mxfp4_experts(x, blocks, scales, experts) ("Quantization" (Linnet docs), format
+    table: "a mixture's chosen experts multiplied from MXFP4, each slot its own input"):
+        y[r, s, n] = sum_k x[r, s, k] * W-hat[experts[r, s], n, k].
+    Each slot is an experts-shared row with one slot.  x bf16 bits [R, S, K].  Returns
+    (y f64 [R, S, N], absdot, bad_slots)."""
+    x = _c(x, np.uint16)
+    r, s, k = x.shape
+    experts = _c(experts, np.int32)
+    y, a, bad = mxfp4_experts_shared(x.reshape(r * s, k), blocks, scales, experts.reshape(r * s, 1), n)
+    return y.reshape(r, s, n), a.reshape(r, s, n), bad
 
 
 def mxfp4_combine_experts(x, blocks, scales, experts, weights, n: int):

@@ -368,6 +368,59 @@ def test_mxfp4_combine_experts_reduces_to_single_slots():
     assert (y3 == 0).all() and (a3 == 0).all()
 
 
+def test_ordered_linear_gathers_inputs_like_scattered_weights():
+    """Int4GroupLinear with an activation order (next row f3): gathering the inputs by
+    `order` must equal scattering the dequantized stored columns back to input positions
+    (stored column j belongs to input order[j]) and multiplying in plain f64, the other
+    way round; identity order gives the plain layer bit for bit; repeated indices add
+    their columns; out-of-range entries are refused."""
+    rng = np.random.default_rng(22)
+    m, n, k, g = 3, 10, 256, 64
+    x = _rand_bf16(rng, (m, k))
+    codes = rng.integers(0, 16, (n, k)).astype(np.uint8)
+    _, packed = oracle.pack_int4(codes, True)
+    scale = (rng.random((n, k // g)) * 0.02 + 0.002).astype(np.float32)
+    zero = rng.integers(0, 16, (n, k // g)).astype(np.uint8)
+    bias = _rand_bf16(rng, (n,))
+    wst = bf16_bits_to_f64(oracle.dequant_int4_groups(packed, scale, zero, n, k, g))
+    xf = bf16_bits_to_f64(x)
+    bf = bf16_bits_to_f64(bias)
+    y0, a0 = oracle.linear_int4_groups(x, packed, scale, zero, bias, n, g)
+    y1, a1 = oracle.linear_int4_groups_ordered(x, np.arange(k), packed, scale, zero, bias, n, g)
+    assert np.array_equal(y0, y1) and np.array_equal(a0, a1)
+    for order in (rng.permutation(k), rng.integers(0, k, k)):  # a permutation, then repeats
+        y, _ = oracle.linear_int4_groups_ordered(x, order, packed, scale, zero, bias, n, g)
+        wnat = np.zeros((n, k))
+        np.add.at(wnat.T, order, wst.T)  # stored column j added to input position order[j]
+        assert np.allclose(y, xf @ wnat.T + bf, rtol=1e-12, atol=1e-12)
+    for bad in (np.full(k, k), np.full(k, -1)):
+        with pytest.raises(ValueError):
+            oracle.linear_int4_groups_ordered(x, bad, packed, scale, zero, bias, n, g)
+
+
+def test_mxfp4_experts_per_slot_inputs():
+    """mxfp4_experts (next row f2, each slot its own input) reduces to
+    mxfp4_experts_shared when every slot of a row gets the row's input, and otherwise
+    to a plain matmul of each slot's input with its expert's dequantized weights."""
+    rng = np.random.default_rng(23)
+    r, e, n, k, s = 2, 5, 6, 64, 3
+    blocks = rng.integers(0, 256, (e, n, k // 32, 16)).astype(np.uint8)
+    scales = rng.integers(118, 125, (e, n, k // 32)).astype(np.uint8)
+    experts = np.array([[4, 0, 2], [1, 1, 3]], np.int32)
+    xr = _rand_bf16(rng, (r, k))
+    ys, _, _ = oracle.mxfp4_experts_shared(xr, blocks, scales, experts, n)
+    yp, _, _ = oracle.mxfp4_experts(np.repeat(xr[:, None, :], s, axis=1), blocks, scales, experts, n)
+    assert np.array_equal(ys, yp)
+    xs = _rand_bf16(rng, (r, s, k))
+    y, _, bad = oracle.mxfp4_experts(xs, blocks, scales, experts, n)
+    assert bad == 0
+    wdq = bf16_bits_to_f64(oracle.dequant_mxfp4(blocks, scales, e, n, k))
+    xf = bf16_bits_to_f64(xs)
+    for rr in range(r):
+        for ss in range(s):
+            assert np.allclose(y[rr, ss], wdq[experts[rr, ss]] @ xf[rr, ss], rtol=0, atol=1e-12)
+
+
 def test_quantization_error_budget():
     """Sanity (not parity): the quantized layer's output stays within the error budget
     of the quantization step (Delta = s/2 plus the bf16 rounding of W-hat) plus f64
