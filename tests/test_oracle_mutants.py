@@ -114,6 +114,7 @@ def real_linear(x, packed, scale, zero, bias, n, group):
 
 
 def test_real_oracle_passes_every_check():
+    from test_oracle_pins import check_dequant_mxfp4
     assert check_l85_int4(real_quantize, real_pack, real_unpack)
     assert check_ch20(real_quantize)
     assert check_int8(real_quantize)
@@ -121,6 +122,36 @@ def test_real_oracle_passes_every_check():
     assert check_nibble_roundtrip(real_pack, real_unpack)
     assert check_dequant_groups(oracle.dequant_int4_groups)
     assert check_linear(real_linear)
+    assert check_dequant_mxfp4(oracle.dequant_mxfp4)
+
+
+def _check_mx(dequant) -> bool:
+    from test_oracle_pins import check_dequant_mxfp4
+    return check_dequant_mxfp4(dequant)
+
+
+def mut_mx_scale_per_16(blocks, scales, e, n, k):       # one scale byte per 16 elements
+    s = np.repeat(scales, 2, -1)[..., : k // 32]
+    return oracle.dequant_mxfp4(blocks, np.ascontiguousarray(s), e, n, k)
+
+
+def mut_mx_scales_transposed(blocks, scales, e, n, k):   # scales stored [E, K/32, N]
+    s = np.ascontiguousarray(scales.reshape(e, k // 32, n).transpose(0, 2, 1))
+    return oracle.dequant_mxfp4(blocks, s, e, n, k)
+
+
+def mut_mx_swapped_nibbles(blocks, scales, e, n, k):     # even element in the high nibble
+    return oracle.dequant_mxfp4(_swap_nibbles(blocks), scales, e, n, k)
+
+
+def mut_mx_bias_128(blocks, scales, e, n, k):            # E8M0 bias 128
+    s = np.where(scales == 255, 255, np.maximum(scales.astype(np.int16) - 1, 0)).astype(np.uint8)
+    return oracle.dequant_mxfp4(blocks, s, e, n, k)
+
+
+def mut_mx_expert_stride(blocks, scales, e, n, k):       # every expert reads expert 0's scales
+    s = np.ascontiguousarray(np.broadcast_to(scales[:1], scales.shape))
+    return oracle.dequant_mxfp4(blocks, s, e, n, k)
 
 
 # ------------------------------------------------------------------ mutants
@@ -224,6 +255,11 @@ def mut_s17_linear(x, packed, scale, zero, bias, n, group):   # W read as [K, N]
     ("m01 scales along the wrong axis", lambda: check_dequant_groups(mut_m01_dequant)),
     ("s16 bias dropped", lambda: check_linear(mut_s16_linear)),
     ("s17 W instead of W^T", lambda: check_linear(mut_s17_linear)),
+    ("mx one scale per 16", lambda: _check_mx(mut_mx_scale_per_16)),
+    ("mx scales transposed over N", lambda: _check_mx(mut_mx_scales_transposed)),
+    ("mx swapped nibbles", lambda: _check_mx(mut_mx_swapped_nibbles)),
+    ("mx E8M0 bias 128", lambda: _check_mx(mut_mx_bias_128)),
+    ("mx expert stride dropped", lambda: _check_mx(mut_mx_expert_stride)),
 ])
 def test_mutant_is_caught(name, check):
     assert not check(), f"planted mistake not caught: {name}"

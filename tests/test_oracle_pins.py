@@ -92,6 +92,61 @@ def test_mxfp4_value_table_and_scale():
     assert (16 + 1) * 8 / int(g["block"][0]) == float(g["bits_per_weight"][0])
 
 
+def mxfp4_torch_restatement(blocks: np.ndarray, scales: np.ndarray) -> torch.Tensor:
+    """dequantize_mxfp4 written again with torch alone ("Quantization" (Linnet docs),
+    format table: E2M1 values in blocks of 32 along K, one E8M0 scale byte a block;
+    "Quantization: int8, int4 group (packed), fp8, KV quant", 2. Principles, MXFP4: the
+    printed magnitudes times the block's power of two): nibbles by torch bit ops (even
+    element low), the printed table by indexing, the block scale by repeat_interleave
+    and torch.ldexp, bias 127, scale byte 255 giving NaN.  Returns f64 [E, N, K]."""
+    g = load("openlearn_l85_mxfp4_values.txt")
+    mags = torch.tensor(floats(g["magnitudes"]), dtype=torch.float64)
+    b = torch.from_numpy(np.ascontiguousarray(blocks)).to(torch.int64)
+    e, n, nb, _ = b.shape
+    nib = torch.stack([b & 15, b >> 4], dim=-1).reshape(e, n, nb * 32)
+    val = mags[nib & 7] * torch.where((nib & 8) != 0, -1.0, 1.0).to(torch.float64)
+    sc = torch.from_numpy(np.ascontiguousarray(scales)).to(torch.int64).repeat_interleave(32, dim=-1)
+    out = torch.ldexp(val, (sc - 127).to(torch.float64))
+    return torch.where(sc == 255, torch.full_like(out, float("nan")), out)
+
+
+def check_dequant_mxfp4(dequant) -> bool:
+    """A dequantizer over several experts, rows and blocks (E = 2, N = 3, K = 128: every
+    scale byte distinct along each axis, codes covering all 16 values in every block) and
+    over the whole E8M0 range 0..255 equals the torch restatement bit for bit (NaN where
+    the scale byte is 255)."""
+    rng = np.random.default_rng(17)
+    e, n, k = 2, 3, 128
+    nibs = np.stack([rng.permutation(16) for _ in range(e * n * (k // 16))]).reshape(e, n, k)
+    blocks = (nibs[..., 0::2] | (nibs[..., 1::2] << 4)).astype(np.uint8).reshape(e, n, k // 32, 16)
+    scales = rng.choice(np.arange(110, 135), size=(e, n, k // 32), replace=False).astype(np.uint8)
+    for sc in (scales, np.arange(256, dtype=np.uint8).reshape(2, 4, 32)):
+        ee, nn, kk = sc.shape[0], sc.shape[1], sc.shape[2] * 32
+        bl = blocks if sc is scales else rng.integers(0, 256, (ee, nn, kk // 32, 16)).astype(np.uint8)
+        got = bf16_bits_to_f64(dequant(bl, sc, ee, nn, kk))
+        want = mxfp4_torch_restatement(bl, sc)
+        want_bf16 = want.to(torch.bfloat16).double().numpy()   # the products are bf16 values
+        if not np.array_equal(got, want_bf16, equal_nan=True):
+            return False
+        if not np.array_equal(np.isnan(got), (np.repeat(sc, 32, -1) == 255)):
+            return False
+    return True
+
+
+def test_dequant_mxfp4_across_experts_rows_and_blocks():
+    """orc_dequant_mxfp4 past one block: the block-scale index (row * K/32 + k/32 over
+    experts and rows) and the nibble order against an independent torch restatement, and
+    the E8M0 reading (bias 127, 255 = NaN) over every scale byte."""
+    assert check_dequant_mxfp4(oracle.dequant_mxfp4)
+    # the E8M0 end points on their own: byte 0 is 2^-127, byte 254 is 2^127, 255 is NaN
+    one = np.full((1, 1, 1, 16), 0x22, np.uint8)            # every code 2: magnitude 1.0
+    for byte, want in ((0, 2.0 ** -127), (127, 1.0), (254, 2.0 ** 127)):
+        v = bf16_bits_to_f64(oracle.dequant_mxfp4(one, np.array([[[byte]]], np.uint8), 1, 1, 32))
+        assert (v == want).all()
+    v = bf16_bits_to_f64(oracle.dequant_mxfp4(one, np.array([[[255]]], np.uint8), 1, 1, 32))
+    assert np.isnan(v).all()
+
+
 # ------------------------------------------------------------------ symmetric quantizer
 def test_zero_group_gets_scale_one():
     w = np.zeros((3, 64), np.float32)
