@@ -116,15 +116,16 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------- oracle leg
-def cpu_oracle_sample(target_s: float = 10.0):
+def cpu_oracle_sample(target_s: float = 10.0, threads: int | None = None):
     """Oracle throughput (GB/s of algorithmic bytes) on a bounded sample of the step:
-    leading rows of each of the seven projections, M = 1, all host cores."""
+    leading rows of each of the seven projections, M = 1, on `threads` host threads (all
+    host cores by default)."""
     import numpy as np
 
     import oracle
     from weight_only_quantized_linear_gb300 import synth
 
-    threads = oracle.max_threads()
+    threads = oracle.max_threads() if threads is None else int(threads)
     oracle.set_threads(threads)
     rng = np.random.default_rng(0)
     rows = 64
@@ -229,7 +230,7 @@ def run_prefill(dev, weights, layers, peaks, stream):
 
         us = time_rotating(call, reps, stream)
         fl = 2.0 * PREFILL_M * N * K
-        per[n] = {"us_per_launch": round(us, 2), "tflops": round(fl / us / 1e6, 1)}
+        per[n] = {"us_per_launch": round(us, 2), "tflops": round(fl / us / 1e6, 1), "kernel": wq.wq_last_launch()}
         tot_flops += fl
         tot_us += us
     dom = max(names, key=lambda n: per[n]["us_per_launch"])
@@ -242,7 +243,7 @@ def run_prefill(dev, weights, layers, peaks, stream):
         "us_per_layer": round(tot_us, 2), "per_projection": per,
         "roofline": {"bound": "tensor", "achieved": round(dom_tf, 1), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(dom_tf / peak, 4), "traffic": load_traffic(f"prefill {dN}x{dK} M={PREFILL_M}"),
-                     "kernel": f"k_gemm_w4g_tc on {dom} {dN}x{dK}, M={PREFILL_M}",
+                     "kernel": f"{per[dom]['kernel']} on {dom} {dN}x{dK}, M={PREFILL_M}",
                      "flops_per_launch": 2 * PREFILL_M * dN * dK,
                      "peak_source": peaks["source"] + " (bf16_tflops, burst: each launch timed alone)"},
         "how": "CUDA events over launches rotating through 32 layers' weights (and 8 activation sets)",
@@ -263,8 +264,7 @@ def run_prefill(dev, weights, layers, peaks, stream):
 
         us = time_rotating(call, reps, stream)
         sweep[str(M)] = {"us": round(us, 2), "gbs": round(proj_bytes(N, K, M) / (us * 1e-6) / 1e9, 1),
-                         "tflops": round(2.0 * M * N * K / us / 1e6, 2),
-                         "regime": "decode GEMV (warp MMA)" if M < 32 else "tcgen05 GEMM"}
+                         "tflops": round(2.0 * M * N * K / us / 1e6, 2), "kernel": wq.wq_last_launch()}
     return prefill, sweep
 
 
@@ -411,6 +411,63 @@ def run_fused_decode(dev, weights, layers, xs, stream, steps, warmup):
                    "same bytes and outputs as the 7-launch step"}
 
 
+def run_stream_ceiling(dev, peaks, stream, reps: int = 20):
+    """The per-launch read ceiling: a kernel that only reads (wq_bench_stream_read), 32
+    launches back to back in a CUDA graph, each over its own buffer (1 GB in all at the
+    largest size, far above L2), at the byte counts of the decode launches (down/gate/up
+    31.69 MB, q/o 9.06 MB, k/v 2.27 MB).  variant 0: plain 16-byte loads; variant 1: a
+    bulk-copy ring per SM that fills before the dependency wait (programmatic dependent
+    launch), as a decode kernel with immutable weights may."""
+    import torch
+
+    import weight_only_quantized_linear_gb300 as wq
+    from weight_only_quantized_linear_gb300 import synth
+
+    sizes = {"31.69 MB (gate/up/down)": proj_bytes(*synth.LLAMA_PROJ["down"]),
+             "9.06 MB (q/o)": proj_bytes(*synth.LLAMA_PROJ["q"]),
+             "2.27 MB (k/v)": proj_bytes(*synth.LLAMA_PROJ["k"])}
+    nbuf = 32
+    big = max(sizes.values())
+    stride = (big + 4095) // 4096 * 4096
+    pool = torch.empty(nbuf * stride, dtype=torch.uint8, device=dev)
+    pool.random_(0, 256)
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = {}
+    for label, nbytes in sizes.items():
+        nb = nbytes // 16 * 16
+        row = {}
+        for variant in (0, 1):
+            def launch_all():
+                for i in range(nbuf):
+                    wq.wq_bench_stream_read(pool[i * stride:], variant, sink, stream=stream, nbytes=nb)
+            with torch.cuda.stream(stream):
+                launch_all()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                launch_all()
+            with torch.cuda.stream(stream):
+                g.replay()
+                torch.cuda.synchronize()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / (reps * nbuf)
+            gbs = nb / (us * 1e-6) / 1e9
+            row["plain_loads" if variant == 0 else "bulk_ring_pdl"] = {
+                "us_per_launch": round(us, 3), "gbs": round(gbs, 1),
+                "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4)}
+        out[label] = row
+    if int(sink.item()) != 0:
+        raise RuntimeError("stream probe wrote its sink")
+    del pool
+    return out
+
+
 def build_weights(dev, layers: int, seed0: int = 1000):
     """Per layer and projection: packed u8 [N, K/2], scale f32 [N, K/G], zero u8 [N, K/G]."""
     import torch
@@ -478,10 +535,13 @@ def run_gpu(args):
             p, s, z = weights[l][n]
             wq.wq_linear_int4_groups(xs[K], p, s, z, None, GROUP, y=ys[(l, n)], workspace=ws[n][l], stream=stream)
 
-    # warm the kernels once outside capture (attributes, descriptors), then capture
+    # warm the kernels once outside capture (attributes, descriptors), then capture; note
+    # the kernel instance the library picks for each projection
+    launched = {}
     with torch.cuda.stream(stream):
         for n in names:
             launch_kind(n)
+            launched[n] = wq.wq_last_launch()
     torch.cuda.synchronize()
     graphs = {}
     for n in names:
@@ -529,6 +589,7 @@ def run_gpu(args):
     prefill = sweep = rows_leg = mxfp4_leg = None
     clocks_p = ClockSampler(dev.index if dev.index is not None else 0)
     clocks_p.start()
+    ceiling = run_stream_ceiling(dev, peaks, stream)
     fused_leg = run_fused_decode(dev, weights, layers, xs, stream, max(10, min(args.steps, 500)), args.warmup)
     if not args.no_prefill:
         prefill, sweep = run_prefill(dev, weights, layers, peaks, stream)
@@ -550,7 +611,8 @@ def run_gpu(args):
     for n in names:
         N, K = synth.LLAMA_PROJ[n]
         us = per_kind_ms[n] / (args.steps * layers) * 1e3
-        per_kind[n] = {"us_per_launch": round(us, 3), "gbs": round(proj_bytes(N, K) / (us * 1e-6) / 1e9, 1)}
+        per_kind[n] = {"us_per_launch": round(us, 3), "gbs": round(proj_bytes(N, K) / (us * 1e-6) / 1e9, 1),
+                       "kernel": launched[n]}
     dom = max(names, key=lambda n: per_kind_ms[n])
     dN, dK = synth.LLAMA_PROJ[dom]
     dom_us = per_kind[dom]["us_per_launch"]
@@ -580,10 +642,37 @@ def run_gpu(args):
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     e2e_value = step_bytes * world / (e2e_ms * 1e-3) / 1e9
 
+    # the same, with every public API call made eagerly each step (no graph): the host
+    # side of the C ABI (validation, tensor maps, launch through ctypes) is inside the
+    # timed region, 224 calls a step
+    eager_steps = max(3, min(args.steps, 200))
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            for n in names:
+                launch_kind(n)
+    torch.cuda.synchronize()
+    h0 = time.perf_counter()
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(eager_steps):
+            for k in xs:
+                xs[k].copy_(x_host[k], non_blocking=True)
+            for n in names:
+                launch_kind(n)
+            for key in last:
+                y_host[key].copy_(ys[key], non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    eager_host_ms = (time.perf_counter() - h0) * 1e3 / eager_steps
+    eager_ms = e0.elapsed_time(e1) / eager_steps
+    eager_value = step_bytes * world / (eager_ms * 1e-3) / 1e9
+
     cpu = None
     if rank == 0 and not args.no_cpu:
         v, threads, sample = cpu_oracle_sample(target_s=args.cpu_seconds)
-        cpu = {"value": round(v, 4), "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample}
+        v1, _, sample1 = cpu_oracle_sample(target_s=max(2.0, args.cpu_seconds / 2), threads=1)
+        cpu = {"value": round(v, 4), "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample,
+               "single_thread": {"value": round(v1, 4), "unit": UNIT, "cores": 1, "sample": sample1}}
 
     if rank == 0:
         line = {
@@ -600,11 +689,17 @@ def run_gpu(args):
             "per_projection": per_kind,
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
-                         "kernel": f"k_gemv<I4G,MT=1> on {dom} {dN}x{dK}",
+                         "kernel": f"{launched[dom]} on {dom} {dN}x{dK}",
                          "bytes_per_launch": proj_bytes(dN, dK), "peak_source": peaks["source"] + " (hbm_gbs)"},
             "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "how": "public API calls captured in CUDA graphs; pinned x copied in and the last layer's "
                            "outputs copied out inside the timed region"},
+            "e2e_eager": {"value": round(eager_value, 1), "unit": UNIT, "ms_per_step": round(eager_ms, 4),
+                          "host_ms_per_step": round(eager_host_ms, 4), "calls_per_step": launches_per_step,
+                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                          "how": "every wq_linear_int4_groups call made through ctypes each step (no graph): "
+                                 "host validation, tensor-map encoding and launch inside the timed region"},
+            "stream_ceiling": ceiling,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
             "cpu_baseline": cpu,

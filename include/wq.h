@@ -81,6 +81,11 @@ WQ_API const char* wq_status_string(int status);
 /* ABI version of this header (major * 100 + minor). */
 WQ_API int wq_version(void);
 
+/* A one-line description of the last compute kernel the calling thread launched through
+ * this library (kernel, template instance, grid); "none" before the first.  The string
+ * belongs to the library and stays valid until the thread's next launch. */
+WQ_API const char* wq_last_launch(void);
+
 /* ------------------------------------------------------------------------------------
  * Group-wise asymmetric 4-bit linear: [Linnet] linear_int4_groups(x, packed, scale,
  * zero, bias) over the Int4GroupLinear layout, "(q - zero) * scale per group"
@@ -150,13 +155,20 @@ WQ_API int wq_set_static_weights(int on);
  * nothing: the split-K scratch it needs lives in one static device array of
  * WQ_NOALLOC_SCRATCH_BYTES inside libwq, which every GPU that loads the library keeps
  * until the process exits.
- *   - Shapes whose split-K scratch would exceed that array are refused with
- *     WQ_EWORKSPACE before anything is launched.
+ *   - Shapes whose split-K scratch would exceed that array run without cross-block
+ *     split-K (the launch wq_linear_int4_groups makes with a NULL workspace: the same
+ *     result up to f32 summation order, slower where N is small).  The decode kernel for
+ *     groups of 128 codes or more needs no scratch at all.
  *   - The first call on a device looks up the array's device address (once per device,
- *     with that device current); make that first call before any stream capture.
- *   - Every call shares the one array: its arrival counters are cleared on the stream
- *     before each launch, and calls whose executions overlap on the GPU (two streams, or
- *     two host threads) race on it.  Serialize them.
+ *     with that device current) and clears the array on the call's stream; make that
+ *     first call before any stream capture.  The cached address outlives a
+ *     cudaDeviceReset: do not reset the device between calls.
+ *   - Every later launch leaves the array's arrival counters at zero again, so nothing
+ *     else runs on the stream between the previous kernel and the launch (wq_set_static_
+ *     weights applies as to wq_linear_int4_groups).  A call that reports WQ_DEV_TIMEOUT
+ *     may leave them non-zero; later results of this entry point are then invalid.
+ *   - Every call shares the one array: calls whose executions overlap on the GPU (two
+ *     streams, or two host threads) race on it.  Serialize them.
  * Results are those of wq_linear_int4_groups.
  * ------------------------------------------------------------------------------------ */
 #define WQ_NOALLOC_SCRATCH_BYTES (1024u * 1024u)
@@ -165,6 +177,50 @@ WQ_API int wq_linear_int4_groups_noalloc(const void* x, int64_t M, int64_t K,
                                          const uint8_t* zero, const int32_t* order,
                                          const void* bias, int64_t N, int32_t group, void* y,
                                          int32_t* dev_status, wq_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * Tuning knobs (the source pages have no counterpart: launch-shape overrides for
+ * measurement and for tests that force each code path).  value 0 restores the library's
+ * own choice; a negative value or an unknown knob returns WQ_EINVAL.  Process-wide;
+ * applies to launches issued after the call.
+ *   WQ_TUNE_GEMV_BLOCKS    thread blocks of the exact decode kernel (groups < 128, MXFP4)
+ *   WQ_TUNE_GEMV_CLUSTERS  thread-block clusters of the factored decode kernel
+ *   WQ_TUNE_GEMV_PUSH      cut-tile fixup of the factored kernel: 1 push, 2 cluster barriers
+ *   WQ_TUNE_GEMV_XSMEM     1: never stage activations in shared memory
+ *   WQ_TUNE_GEMM_MIN_M     smallest M that takes the tensor-core GEMM (default 32)
+ * ------------------------------------------------------------------------------------ */
+enum {
+  WQ_TUNE_GEMV_BLOCKS = 0,
+  WQ_TUNE_GEMV_CLUSTERS = 1,
+  WQ_TUNE_GEMV_PUSH = 2,
+  WQ_TUNE_GEMV_XSMEM = 3,
+  WQ_TUNE_GEMM_MIN_M = 4
+};
+WQ_API int wq_set_tuning(int32_t knob, int64_t value);
+
+/* ------------------------------------------------------------------------------------
+ * Test and measurement exports (no counterpart in the source pages).
+ *
+ * wq_test_wait_timeout: launches one warp that waits on a shared-memory barrier with the
+ * same bounded wait every kernel of the library uses, limited to limit_ns (1 ..
+ * 100000000, else WQ_EINVAL).  arrive != 0: the warp arrives first and the wait succeeds;
+ * arrive == 0: nobody arrives, the wait gives up after limit_ns, WQ_DEV_TIMEOUT is OR-ed
+ * into *dev_status and the kernel returns.  Nothing else is in flight when it gives up,
+ * so the context stays usable: it shows the failure path without a fault.
+ *
+ * wq_bench_stream_read: reads `bytes` (rounded down to a multiple of 16) of the device
+ * buffer `buf` and does nothing else: the per-launch HBM read rate a kernel without any
+ * arithmetic reaches.  variant 0: plain 16-byte loads, eight in flight a thread, 8 blocks
+ * of 256 threads an SM; variant 1: one block an SM streaming its share through a
+ * six-stage ring of 16 KB bulk copies, launched with programmatic dependent launch and
+ * filling its ring before waiting for the previous kernel of the stream (buf must not be
+ * written by that kernel).  *sink (device u32) is written only in the impossible case
+ * that the folded words equal a fixed constant.
+ * ------------------------------------------------------------------------------------ */
+WQ_API int wq_test_wait_timeout(uint64_t limit_ns, int32_t arrive, int32_t* dev_status,
+                                wq_stream_t stream);
+WQ_API int wq_bench_stream_read(const void* buf, size_t bytes, int32_t variant, uint32_t* sink,
+                                wq_stream_t stream);
 
 /* ------------------------------------------------------------------------------------
  * Symmetric per-row int8 linear: [Linnet] Int8Linear<In, Out, T> (weight [Out, In; i8],

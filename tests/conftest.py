@@ -21,3 +21,19 @@ def cuda_device():
     if not torch.cuda.is_available():
         pytest.fail("test marked gpu but no CUDA device is visible")
     return torch.device("cuda:0")
+
+
+@pytest.fixture
+def tune():
+    """Set launch-shape knobs (wq_set_tuning) for one test; every knob it touched is
+    restored to the library's own choice afterwards."""
+    import weight_only_quantized_linear_gb300 as wq
+    touched = []
+
+    def set_knob(knob, value):
+        wq.wq_set_tuning(knob, value)
+        touched.append(knob)
+
+    yield set_knob
+    for k in touched:
+        wq.wq_set_tuning(k, 0)

@@ -116,7 +116,7 @@ def test_int4_groups_zero_points_over_full_byte_range(cuda_device, M, G):
     assert_within(y, yr, ad, f"full-range zero points M={M} G={G}")
 
 
-def test_int4_groups_deterministic_and_split_invariant(cuda_device, monkeypatch):
+def test_int4_groups_deterministic_and_split_invariant(cuda_device):
     d = cuda_device
     M, N, K, G = 1, 1024, 4096, 128
     packed, scale, zero = make_i4g(N, K, G, seed=3)
@@ -268,13 +268,13 @@ def test_mxfp4_many_rows_per_expert_and_bad_index(cuda_device):
 
 @pytest.mark.parametrize("grid", [1, 3, 7, 64, 151])
 @pytest.mark.parametrize("M", [1, 13])
-def test_stream_k_partitions(cuda_device, monkeypatch, grid, M):
+def test_stream_k_partitions(cuda_device, tune, grid, M):
     """Every block (exact kernel) or cluster (factored kernel) count gives the same
     answer: tiles cut anywhere by the equal-share ranges are finished from their partials
     (deterministically)."""
     d = cuda_device
-    monkeypatch.setenv("WQ_GEMV_BLOCKS", str(grid))
-    monkeypatch.setenv("WQ_GEMV_CLUSTERS", str(grid))
+    tune(wq.WQ_TUNE_GEMV_BLOCKS, grid)
+    tune(wq.WQ_TUNE_GEMV_CLUSTERS, grid)
     N, K, G = 1000, 4096 + 1024, 128
     packed, scale, zero = make_i4g(N, K, G, seed=grid)
     x = synth.normal_bf16((M, K), seed=grid + 1)
@@ -286,16 +286,16 @@ def test_stream_k_partitions(cuda_device, monkeypatch, grid, M):
     assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
 
 
-def test_gemm_matches_gemv_path(cuda_device, monkeypatch):
+def test_gemm_matches_gemv_path(cuda_device, tune):
     """The tensor-core regime and the decode regime agree (both within the oracle's
-    tolerance); the crossover moves with WQ_GEMM_MIN_M."""
+    tolerance); the crossover moves with the WQ_TUNE_GEMM_MIN_M knob."""
     d = cuda_device
     M, N, K, G = 48, 512, 2048, 128
     packed, scale, zero = make_i4g(N, K, G, seed=77)
     x = dev(synth.normal_bf16((M, K), seed=78), d)
     args = (dev(packed, d), dev(scale, d), dev(zero, d))
     y_tc = run_i4g(d, x, *args, None, G)
-    monkeypatch.setenv("WQ_GEMM_MIN_M", "100000")
+    tune(wq.WQ_TUNE_GEMM_MIN_M, 100000)
     y_gemv = run_i4g(d, x, *args, None, G)
     yr, ad = oracle.linear_int4_groups(bf16_bits(x.cpu()), packed, scale, zero, None, N, G)
     assert_within(y_tc, yr, ad, "tcgen05")
@@ -361,11 +361,11 @@ def test_static_weights_same_result(cuda_device, M, N, K):
 
 @pytest.mark.parametrize("xsmem", ["1", "0"])
 @pytest.mark.parametrize("M,N,K", [(1, 4096, 14336), (3, 1000, 4096), (8, 300, 2048)])
-def test_factored_activation_paths(cuda_device, monkeypatch, xsmem, M, N, K):
+def test_factored_activation_paths(cuda_device, tune, xsmem, M, N, K):
     """Activations staged in shared memory (the default where two blocks an SM still fit,
     with a three-stage ring at K = 14336) and read from global memory give results
     within the tolerance."""
-    monkeypatch.setenv("WQ_GEMV_XSMEM", xsmem)
+    tune(wq.WQ_TUNE_GEMV_XSMEM, 0 if xsmem == "1" else 1)
     d = cuda_device
     G = 128
     packed, scale, zero = make_i4g(N, K, G, seed=K + M)
@@ -410,17 +410,17 @@ def test_decode_offset_activations_full_range_zero_points(cuda_device, M, fmt):
 @pytest.mark.parametrize("M,N,K,clusters", [(1, 14336, 4096, None), (1, 4096, 14336, None), (1, 1024, 4096, None),
                                             (1, 4096, 4096, None), (4, 1000, 6144, 5), (12, 700, 4096, None),
                                             (1, 256, 2048, 3)])
-def test_factored_cut_tile_fixup(cuda_device, monkeypatch, mode, M, N, K, clusters):
+def test_factored_cut_tile_fixup(cuda_device, tune, mode, M, N, K, clusters):
     """Tiles cut between warps are finished either by pushes into the closing warp's
     shared memory (no cluster-wide barrier) or by the closing warp reading the parked
     partials after cluster barriers (forced each way, and the launch's own choice); all
     match the oracle and are deterministic."""
     if mode == "push":
-        monkeypatch.setenv("WQ_GEMV_PUSH", "1")
+        tune(wq.WQ_TUNE_GEMV_PUSH, 1)
     elif mode == "barrier":
-        monkeypatch.setenv("WQ_GEMV_PUSH", "0")
+        tune(wq.WQ_TUNE_GEMV_PUSH, 2)
     if clusters is not None:
-        monkeypatch.setenv("WQ_GEMV_CLUSTERS", str(clusters))
+        tune(wq.WQ_TUNE_GEMV_CLUSTERS, clusters)
     d = cuda_device
     G = 128
     packed, scale, zero = make_i4g(N, K, G, seed=N + M)

@@ -52,14 +52,47 @@ def test_noalloc_matches_workspace_entry_point_twice(cuda_device, M, N, K, G):
     assert torch.equal(y2.view(torch.int16), y_ref.view(torch.int16))
 
 
-def test_noalloc_refuses_shapes_beyond_its_scratch(cuda_device):
+@pytest.mark.parametrize("M,N,K,G", [(16, 14336, 4096, 128), (16, 14336, 4096, 64)])
+def test_noalloc_large_decode_shapes_run_without_split(cuda_device, M, N, K, G):
+    """The Llama gate shape at M = 16.  Group 128 takes the decode kernel that needs no
+    scratch; group 64 takes the exact kernel, whose split-K scratch for this shape is
+    larger than the static array, so the call runs it without cross-block split-K (as
+    wq_linear_int4_groups does with a NULL workspace) instead of refusing."""
     d = cuda_device
-    M, N, K, G = 1, 6_000_000, 32, 32       # 375000 tiles: counters alone exceed the array
-    x, packed, scale, zero, _ = _inputs(1, 16, K, G, seed=5, d=d)
-    big_packed = torch.zeros((N, K // 2), dtype=torch.uint8, device=d)
-    big_scale = torch.ones((N, K // G), dtype=torch.float32, device=d)
-    big_zero = torch.zeros((N, K // G), dtype=torch.uint8, device=d)
-    assert wq.wq_linear_int4_groups_workspace(M, N, K, G) > 1024 * 1024
-    with pytest.raises(wq.WQError) as e:
-        wq.wq_linear_int4_groups_noalloc(x, big_packed, big_scale, big_zero, None, G)
-    assert e.value.status == wq.WQ_EWORKSPACE
+    x, packed, scale, zero, bias = _inputs(M, N, K, G, seed=M + N + G, d=d)
+    y1 = wq.wq_linear_int4_groups_noalloc(x, packed, scale, zero, bias, G)
+    y2 = wq.wq_linear_int4_groups_noalloc(x, packed, scale, zero, bias, G)
+    y_nows = wq.wq_linear_int4_groups(x, packed, scale, zero, bias, G)
+    torch.cuda.synchronize()
+    if G == 64:
+        assert wq.wq_linear_int4_groups_workspace(M, N, K, G) > 1024 * 1024
+    assert torch.equal(y1.view(torch.int16), y_nows.view(torch.int16))
+    assert torch.equal(y2.view(torch.int16), y_nows.view(torch.int16))
+    rows = np.random.default_rng(G).choice(N, 256, replace=False)
+    rows.sort()
+    yr, ad = oracle.linear_int4_groups(bf16_bits(x), packed.cpu().numpy()[rows], scale.cpu().numpy()[rows],
+                                       zero.cpu().numpy()[rows], bf16_bits(bias)[rows], len(rows), G)
+    assert_within(y1[:, torch.from_numpy(rows).to(d)], yr, ad, f"noalloc M={M} G={G}")
+
+
+def test_noalloc_allocates_no_device_memory(cuda_device):
+    """After a first call (which sets up the static array), further calls with a
+    preallocated output change neither torch's allocator nor the device's free bytes."""
+    d = cuda_device
+    M, N, K, G = 2, 1000, 4096, 64                  # the exact kernel, split-K through the array
+    x, packed, scale, zero, bias = _inputs(M, N, K, G, seed=9, d=d)
+    assert 0 < wq.wq_linear_int4_groups_workspace(M, N, K, G) <= 1024 * 1024
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=d)
+    wq.wq_linear_int4_groups_noalloc(x, packed, scale, zero, bias, G, y=y)
+    torch.cuda.synchronize()
+    y_first = y.clone()
+    torch.cuda.synchronize()
+    alloc0 = torch.cuda.memory_allocated(d)
+    free0, _ = torch.cuda.mem_get_info(d)
+    for _ in range(3):
+        wq.wq_linear_int4_groups_noalloc(x, packed, scale, zero, bias, G, y=y)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info(d)
+    assert torch.cuda.memory_allocated(d) == alloc0
+    assert free1 == free0
+    assert torch.equal(y.view(torch.int16), y_first.view(torch.int16))

@@ -21,6 +21,8 @@ HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "wq.h")
 WQ_OK, WQ_EINVAL, WQ_ESHAPE, WQ_EALIGN, WQ_ERANGE, WQ_EUNSUPPORTED, WQ_ECUDA, WQ_EWORKSPACE = range(8)
 WQ_DEV_NONFINITE, WQ_DEV_BAD_EXPERT, WQ_DEV_BAD_CODE, WQ_DEV_TIMEOUT = 1, 2, 4, 8
 WQ_SYM, WQ_SYM_U4, WQ_ASYM = 0, 1, 2
+(WQ_TUNE_GEMV_BLOCKS, WQ_TUNE_GEMV_CLUSTERS, WQ_TUNE_GEMV_PUSH, WQ_TUNE_GEMV_XSMEM,
+ WQ_TUNE_GEMM_MIN_M) = range(5)
 
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
@@ -30,10 +32,14 @@ _SZ = ctypes.c_size_t
 SIGNATURES = {
     "wq_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "wq_version": (ctypes.c_int, []),
+    "wq_last_launch": (ctypes.c_char_p, []),
     "wq_linear_int4_groups": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P, _P, _P, _I64, _I32, _P, _P, _SZ,
                                              _P, _P]),
     "wq_linear_int4_groups_workspace": (_SZ, [_I64, _I64, _I64, _I32]),
     "wq_set_static_weights": (ctypes.c_int, [ctypes.c_int]),
+    "wq_set_tuning": (ctypes.c_int, [_I32, _I64]),
+    "wq_test_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, _I32, _P, _P]),
+    "wq_bench_stream_read": (ctypes.c_int, [_P, _SZ, _I32, _P, _P]),
     "wq_linear_int4_groups_noalloc": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P, _P, _P, _I64, _I32, _P,
                                                      _P, _P]),
     "wq_linear_int8_rows": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P, _I64, _P, _P, _SZ, _P, _P]),
@@ -88,6 +94,11 @@ def status_string(status: int) -> str:
     return lib().wq_status_string(int(status)).decode()
 
 
+def wq_last_launch() -> str:
+    """The last compute kernel this thread launched through the library (see wq.h)."""
+    return lib().wq_last_launch().decode()
+
+
 def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
@@ -134,6 +145,25 @@ def wq_set_static_weights(on: bool) -> None:
     work while calls read them (see wq.h): the decode kernel may then start streaming
     them before the previous kernel of the stream has completed."""
     _check(lib().wq_set_static_weights(1 if on else 0), "wq_set_static_weights")
+
+
+def wq_set_tuning(knob: int, value: int) -> None:
+    """Override one launch-shape choice (WQ_TUNE_*); 0 restores the library's own."""
+    _check(lib().wq_set_tuning(int(knob), int(value)), "wq_set_tuning")
+
+
+def wq_test_wait_timeout(limit_ns: int, arrive: bool, dev_status, stream=None) -> None:
+    """One warp waits on a barrier with the library's bounded wait (see wq.h)."""
+    _need(dev_status, torch.int32, "dev_status")
+    _check(lib().wq_test_wait_timeout(int(limit_ns), 1 if arrive else 0, _ptr(dev_status), _stream(stream)),
+           "wq_test_wait_timeout")
+
+
+def wq_bench_stream_read(buf, variant: int, sink, stream=None, nbytes: int | None = None) -> None:
+    """Read the device buffer and do nothing else (the per-launch read ceiling)."""
+    n = buf.numel() * buf.element_size() if nbytes is None else int(nbytes)
+    _check(lib().wq_bench_stream_read(_ptr(buf), n, int(variant), _ptr(sink), _stream(stream)),
+           "wq_bench_stream_read")
 
 
 def alloc_workspace(nbytes: int, device) -> torch.Tensor | None:

@@ -6,6 +6,8 @@
 // synchronizes, allocates device memory or throws.
 #include <cudaTypedefs.h>
 
+#include <cstdarg>
+#include <cstdio>
 #include <mutex>
 
 #include "../../include/wq.h"
@@ -82,7 +84,17 @@ int check_rows_common(const void* x, int64_t M, int64_t K, const void* w, const 
   return WQ_OK;
 }
 
+thread_local char t_last_launch[256] = "none";
+
 }  // namespace
+
+void note_launch(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_last_launch, sizeof(t_last_launch), fmt, ap);
+  va_end(ap);
+}
+const char* last_launch() { return t_last_launch; }
 
 bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, void* base,
                           uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
@@ -119,9 +131,35 @@ WQ_API const char* wq_status_string(int status) {
 
 WQ_API int wq_version(void) { return 100; }
 
+WQ_API const char* wq_last_launch(void) { return last_launch(); }
+
 WQ_API int wq_set_static_weights(int on) {
   set_static_weights(on);
   return WQ_OK;
+}
+
+WQ_API int wq_set_tuning(int32_t knob, int64_t value) {
+  return set_tuning(knob, value) ? WQ_OK : WQ_EINVAL;
+}
+
+WQ_API int wq_test_wait_timeout(uint64_t limit_ns, int32_t arrive, int32_t* dev_status,
+                                wq_stream_t stream) {
+  if (limit_ns == 0 || limit_ns > 100000000ull) return WQ_EINVAL;
+  return launch_wait_probe(limit_ns, arrive, dev_status, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? WQ_OK
+             : WQ_ECUDA;
+}
+
+WQ_API int wq_bench_stream_read(const void* buf, size_t bytes, int32_t variant, uint32_t* sink,
+                                wq_stream_t stream) {
+  if (!buf || !sink || bytes < 16) return WQ_EINVAL;
+  if (variant != 0 && variant != 1) return WQ_EINVAL;
+  if (!aligned(buf, 16) || !aligned(sink, 4)) return WQ_EALIGN;
+  return launch_stream_read(buf, (int64_t)(bytes & ~size_t(15)), variant, sink, num_sms_current(),
+                            reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? WQ_OK
+             : WQ_ECUDA;
 }
 
 // ------------------------------------------------------------------ group-wise 4-bit
@@ -179,14 +217,17 @@ WQ_API int wq_linear_int4_groups(const void* x, int64_t M, int64_t K, const uint
 // ------------------------------------------------------------------ allocation-free variant
 // Scratch for callers that cannot allocate device memory (see wq.h): one static array a
 // GPU, its device address looked up once per device with cudaGetSymbolAddress (the
-// host-side name of the array is only a stand-in and must never reach a kernel).
+// host-side name of the array is only a stand-in and must never reach a kernel).  The
+// set-up also clears the array once on the caller's stream; from then on every launch
+// leaves its arrival counters at zero, so no per-call clearing stands between the
+// previous kernel and the next launch.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[WQ_NOALLOC_SCRATCH_BYTES];
 
 namespace {
 std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[kMaxDevices] = {nullptr};
 
-int noalloc_scratch(void** out) {
+int noalloc_scratch(void** out, cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return WQ_ECUDA;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
@@ -194,6 +235,7 @@ int noalloc_scratch(void** out) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
       return WQ_ECUDA;
+    if (cudaMemsetAsync(p, 0, WQ_NOALLOC_SCRATCH_BYTES, stream) != cudaSuccess) return WQ_ECUDA;
     g_noalloc_ptr[dev] = p;
   }
   *out = g_noalloc_ptr[dev];
@@ -217,18 +259,14 @@ WQ_API int wq_linear_int4_groups_noalloc(const void* x, int64_t M, int64_t K,
     return wq_linear_int4_groups(x, M, K, packed, scale, zero, order, bias, N, group, y,
                                  nullptr, 0, dev_status, stream);
   const size_t need = wq_linear_int4_groups_workspace(M, N, K, group);
-  if (need == 0)  // this shape runs without scratch
+  // shapes that run without scratch, and shapes whose split-K scratch would not fit the
+  // array, take the launch without cross-block split-K (same result up to f32 order)
+  if (need == 0 || need > WQ_NOALLOC_SCRATCH_BYTES)
     return wq_linear_int4_groups(x, M, K, packed, scale, zero, order, bias, N, group, y,
                                  nullptr, 0, dev_status, stream);
-  if (need > WQ_NOALLOC_SCRATCH_BYTES) return WQ_EWORKSPACE;
   void* scratch = nullptr;
-  st = noalloc_scratch(&scratch);
+  st = noalloc_scratch(&scratch, reinterpret_cast<cudaStream_t>(stream));
   if (st != WQ_OK) return st;
-  // the arrival counters must start at zero; the array keeps the last call's contents
-  const GemvPlan pl = plan_gemv(Fmt::I4G, M, N, K, num_sms_current());
-  if (cudaMemsetAsync(scratch, 0, ws_counter_bytes(pl.tiles),
-                      reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return WQ_ECUDA;
   return wq_linear_int4_groups(x, M, K, packed, scale, zero, order, bias, N, group, y, scratch,
                                need, dev_status, stream);
 }

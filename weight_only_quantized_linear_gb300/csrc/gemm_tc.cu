@@ -177,6 +177,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       tma_prefetch_desc(&xmap);
       tma_prefetch_desc(&pmap);
       const uint64_t pol = l2_policy_evict_last();  // x and W tiles are re-read by other blocks
+      int issued = 0;
       for (int kb = 0; kb < nk; ++kb) {
         const int s = kb % kStagesTc;
         if (kb >= kStagesTc && !mbar_wait(&sh->empty[s], ((kb / kStagesTc) - 1) & 1)) {
@@ -188,7 +189,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         mbar_arrive_expect_tx(&sh->full_tma[s], kABytes + kPBytes);
         tma_load_2d(stage_a(s), &xmap, &sh->full_tma[s], (kb0 + kb) * kBK, (int32_t)m0, pol);
         tma_load_2d(stage_p(s), &pmap, &sh->full_tma[s], (kb0 + kb) * (kBK / 2), (int32_t)n0, pol);
+        issued = kb + 1;
       }
+      // no copy may land in shared memory after the block exits: wait (bounded) for the
+      // last copy issued into each stage (long complete unless the block is aborting)
+      for (int kb = std::max(0, issued - kStagesTc); kb < issued; ++kb)
+        (void)mbar_wait(&sh->full_tma[kb % kStagesTc], (uint32_t)(kb / kStagesTc) & 1u);
     }
   } else if (warp == 1) {
     // ================= MMA issuer =================
@@ -465,11 +471,8 @@ size_t gemm_tc_ws_bytes(int64_t M, int64_t N, int64_t K, int num_sms) {
 }
 
 bool gemm_tc_supported(int64_t M, int64_t N, int64_t K, int32_t group) {
-  if (const char* env = std::getenv("WQ_GEMM_MIN_M")) {  // tuning knob for the crossover
-    if (M < std::atoll(env)) return false;
-  } else if (M < 32) {
-    return false;
-  }
+  const int64_t min_m = tuning(kKnobGemmMinM);  // tuning and test knob for the crossover
+  if (M < (min_m >= 1 ? min_m : 32)) return false;
   return N >= 1 && K >= 32 && K % 32 == 0 && (group == 32 || group == 64 || group == 128 ||
                                                group == 256) &&
          K % group == 0 && M <= (int64_t(1) << 31) && N <= (int64_t(1) << 31);
@@ -505,6 +508,8 @@ cudaError_t launch_gemm_tc(const GemmTcParams& p, int num_sms, cudaStream_t stre
   if (splits == 1) q.part = nullptr;
   const dim3 grid((unsigned)((p.M + kBM - 1) / kBM), (unsigned)((p.N + kBN - 1) / kBN),
                   (unsigned)splits);
+  note_launch("k_gemm_w4g_tc<%s> grid=%ux%ux%u%s", splits > 1 ? "split" : "unsplit", grid.x, grid.y,
+              grid.z, splits > 1 ? " + k_splitk_reduce" : "");
   if (splits == 1)
     k_gemm_w4g_tc<false><<<grid, kThreadsTc, smem, stream>>>(xmap, pmap, q);
   else

@@ -962,12 +962,14 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
   uint32_t phase = 0;
   for (int u = 0; u < total; ++u) {
     if (!mbar_wait(bars + stage, phase)) {
-      // the copy never completed: record it, wait (bounded) for the other copies this
-      // warp has in flight, and give up on its range (the cluster barriers below are
-      // still reached by every thread)
+      // the copy never completed: record it and give up on the warp's range (the
+      // cluster barriers below are still reached by every thread).  Before leaving, wait
+      // again (bounded) for every copy the warp has in flight: units u .. u + kS - 2,
+      // the one that timed out included, so that no copy lands in shared memory after
+      // the block may have exited.
       if (lane == 0) {
         set_dev_status(p.dev_status, WQ_DEV_TIMEOUT);
-        for (int v = u + 1; v < total && v <= u + kS - 2; ++v)
+        for (int v = u; v < total && v <= u + kS - 2; ++v)
           (void)mbar_wait(bars + v % kS, (uint32_t)(v / kS) & 1u);
       }
       __syncwarp();
@@ -1177,19 +1179,21 @@ bool fact_ok(Fmt f, const GemvParams& p) {
 // ------------------------------------------------------------------ host side
 namespace {
 
+constexpr const char* fmt_name(Fmt f) {
+  return f == Fmt::I4G ? "I4G" : (f == Fmt::I4R ? "I4R" : (f == Fmt::I8R ? "I8R" : "MXFP4"));
+}
+
 template <Fmt F, int MT, bool FMA>
 cudaError_t launch_t(const GemvParams& p, int grid, cudaStream_t stream) {
   const size_t smem = (F == Fmt::MXFP4) ? sizeof(Routing) : 0;
+  note_launch("k_gemv<%s,MT=%d,%s> grid=%d%s", fmt_name(F), MT, FMA ? "FMA" : "MMA", grid,
+              p.ws_cnt ? " stream-K" : "");
   k_gemv<F, MT, FMA><<<grid, kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
 // The factored kernel runs in clusters of kFactCluster CTAs, as many clusters as fit on
 // the GPU at once (one wave), never more than there are items.
-bool env_disabled(const char* name) {  // test knob: NAME=0 turns a path off
-  const char* v = std::getenv(name);
-  return v != nullptr && v[0] == '0';
-}
 template <Fmt F>
 constexpr int kChunkK() { return chunk_k<F>(); }
 constexpr int kFactMinSteps = 2;
@@ -1202,7 +1206,7 @@ constexpr size_t kFactStaticBytes = (size_t)kWarps * 2 * 32 * 4 * sizeof(float);
 
 template <Fmt F, int MT, int kSD, bool kXS, bool kPush>
 cudaError_t launch_fact_t(const GemvParams& p, const FactMaps& maps, const FactGeom& geo,
-                          size_t smem, int64_t clusters, cudaStream_t stream) {
+                          size_t smem, int64_t clusters, int num_sms, cudaStream_t stream) {
   // co-resident clusters a device for the last dynamic shared-memory size (0: unknown)
   static int active[kMaxDevicesGemv] = {0};
   static size_t active_smem[kMaxDevicesGemv] = {0};
@@ -1233,12 +1237,12 @@ cudaError_t launch_fact_t(const GemvParams& p, const FactMaps& maps, const FactG
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (active[dev] == 0 || active_smem[dev] != smem) {
-    cfg.gridDim = dim3(kFactCluster * kNumSMsFallback);
+    cfg.gridDim = dim3(kFactCluster * (unsigned)num_sms);
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, k_gemv_fact<F, MT, kSD, kXS, kPush>, &cfg) != cudaSuccess ||
         n <= 0) {
       (void)cudaGetLastError();
-      n = kNumSMsFallback * kBlocksPerSM / kFactCluster;
+      n = num_sms * kBlocksPerSM / kFactCluster;
     }
     active[dev] = n;
     active_smem[dev] = smem;
@@ -1246,6 +1250,9 @@ cudaError_t launch_fact_t(const GemvParams& p, const FactMaps& maps, const FactG
   if (clusters > active[dev]) clusters = active[dev];  // one wave (the caller sized it)
   cfg.gridDim = dim3((unsigned)(std::max<int64_t>(1, clusters) * kFactCluster));
   cfg.numAttrs = 2;
+  note_launch("k_gemv_fact<%s,MT=%d,stages=%d,%s,%s> grid=%u (%lld clusters of %d) smem=%zu",
+              fmt_name(F), MT, kSD, kXS ? "x staged" : "x global", kPush ? "push fixup" : "barrier fixup",
+              cfg.gridDim.x, (long long)std::max<int64_t>(1, clusters), kFactCluster, smem);
   return cudaLaunchKernelEx(&cfg, k_gemv_fact<F, MT, kSD, kXS, kPush>, p, maps, geo);
 }
 
@@ -1253,7 +1260,7 @@ cudaError_t launch_fact_t(const GemvParams& p, const FactMaps& maps, const FactG
 // memory (4-bit formats, up to 8 rows) when two blocks an SM still fit, with the ring cut
 // to three stages if that is what makes them fit (K = 14336 at one row).
 template <Fmt F, int MT>
-cudaError_t launch_fact(const GemvParams& p, cudaStream_t stream) {
+cudaError_t launch_fact(const GemvParams& p, int num_sms, cudaStream_t stream) {
   // tensor maps of codes, scales and zero points
   FactMaps maps;
   const int64_t row_bytes = (F == Fmt::I8R) ? p.K : p.K / 2;
@@ -1285,12 +1292,9 @@ cudaError_t launch_fact(const GemvParams& p, cudaStream_t stream) {
   // Nine tenths of the clusters two blocks an SM would hold: measured on GB300, 34 clusters
   // of 8 beat 36 to 38 by 4 to 10 % on the 14336 x 4096 and 4096 x 14336 layers (with 36
   // or more, the last clusters of a launch start late).
-  int64_t cap = std::min<int64_t>(kNumSMsFallback * kBlocksPerSM * 9 / (10 * kFactCluster),
+  int64_t cap = std::min<int64_t>((int64_t)num_sms * kBlocksPerSM * 9 / (10 * kFactCluster),
                                   std::max<int64_t>(1, items * spt / (kFactWarps * kFactMinSteps)));
-  if (const char* env = std::getenv("WQ_GEMV_CLUSTERS")) {  // tuning and test knob
-    const int v = std::atoi(env);
-    if (v >= 1) cap = v;
-  }
+  if (const int64_t v = tuning(kKnobGemvClusters); v >= 1) cap = v;  // tuning and test knob
   const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(cap, items));
   // push fixup: receive slots a warp = the most warps any cut tile meets, from the same
   // split as the kernel (cluster c takes q or q + 1 items; warp w of a cluster starts at
@@ -1316,39 +1320,39 @@ cudaError_t launch_fact(const GemvParams& p, cudaStream_t stream) {
   const size_t recv = (size_t)kWarps * cmax * 16 * (size_t)p.M * 4 + kWarps * 8;
   // the push fixup pays where few warps share a tile (the closing warp waits for each in
   // turn); with many (long rows or small N) the cluster barriers do better, as measured
-  const char* push_env = std::getenv("WQ_GEMV_PUSH");  // test knob: 1 forces it, 0 disables it
-  const bool push_ok = push_env ? (push_env[0] == '1' && cmax <= 32) : (cmax <= 4);
+  const int64_t push_knob = tuning(kKnobGemvPush);  // test knob: 1 forces it, 2 disables it
+  const bool push_ok = push_knob == 1 ? cmax <= 32 : (push_knob == 2 ? false : cmax <= 4);
   // two blocks an SM: (dynamic + static + the 1 KB the driver reserves) twice
   auto fits = [&](size_t dyn) { return 2 * (dyn + kFactStaticBytes + 1024) <= kSmemPerSMFact; };
   if constexpr (F != Fmt::I8R && MT == 1) {
-    const bool x_ok = !env_disabled("WQ_GEMV_XSMEM") && p.K % kChunkK<F>() == 0 &&
+    const bool x_ok = tuning(kKnobGemvXsmem) != 1 && p.K % kChunkK<F>() == 0 &&
                       (reinterpret_cast<uintptr_t>(p.x) % 16) == 0;
     const uint32_t xstride = (uint32_t)(p.M > 1 ? p.K * 2 + kFactXPad : p.K * 2);
     const size_t xbytes = ((size_t)p.M * xstride + 15) & ~size_t(15);
     const FactGeom geo{xstride, cmax};
     if (x_ok && push_ok && fits(ring4 + xbytes + recv))
-      return launch_fact_t<F, MT, 4, true, true>(p, maps, geo, ring4 + xbytes + recv, clusters, stream);
+      return launch_fact_t<F, MT, 4, true, true>(p, maps, geo, ring4 + xbytes + recv, clusters, num_sms, stream);
     if (x_ok && push_ok && fits(ring3 + xbytes + recv))
-      return launch_fact_t<F, MT, 3, true, true>(p, maps, geo, ring3 + xbytes + recv, clusters, stream);
+      return launch_fact_t<F, MT, 3, true, true>(p, maps, geo, ring3 + xbytes + recv, clusters, num_sms, stream);
     if (x_ok && fits(ring4 + xbytes))
-      return launch_fact_t<F, MT, 4, true, false>(p, maps, geo, ring4 + xbytes, clusters, stream);
+      return launch_fact_t<F, MT, 4, true, false>(p, maps, geo, ring4 + xbytes, clusters, num_sms, stream);
     if (x_ok && fits(ring3 + xbytes))
-      return launch_fact_t<F, MT, 3, true, false>(p, maps, geo, ring3 + xbytes, clusters, stream);
+      return launch_fact_t<F, MT, 3, true, false>(p, maps, geo, ring3 + xbytes, clusters, num_sms, stream);
   }
   const FactGeom geo{0, cmax};
   if (push_ok && fits(ring4 + recv))
-    return launch_fact_t<F, MT, 4, false, true>(p, maps, geo, ring4 + recv, clusters, stream);
-  return launch_fact_t<F, MT, 4, false, false>(p, maps, geo, ring4, clusters, stream);
+    return launch_fact_t<F, MT, 4, false, true>(p, maps, geo, ring4 + recv, clusters, num_sms, stream);
+  return launch_fact_t<F, MT, 4, false, false>(p, maps, geo, ring4, clusters, num_sms, stream);
 }
 
 // I4G with a group of at least 128 codes, I4R, I8R: the factored kernel (warp MMA,
 // batches of 8 or 16 activation rows).  I4G with smaller groups and MXFP4: the exact
 // kernel, on the FMA pipe for one or two rows and on the warp MMA for more.
 template <Fmt F>
-cudaError_t launch_f(const GemvParams& p, int64_t rows, int grid, cudaStream_t stream) {
+cudaError_t launch_f(const GemvParams& p, int64_t rows, int grid, int num_sms, cudaStream_t stream) {
   if constexpr (F != Fmt::MXFP4) {
     if (fact_ok(F, p))
-      return rows <= 8 ? launch_fact<F, 1>(p, stream) : launch_fact<F, 2>(p, stream);
+      return rows <= 8 ? launch_fact<F, 1>(p, num_sms, stream) : launch_fact<F, 2>(p, num_sms, stream);
   }
   if (rows <= 1) return launch_t<F, 1, true>(p, grid, stream);
   if (rows <= 2) return launch_t<F, 2, true>(p, grid, stream);
@@ -1360,23 +1364,31 @@ cudaError_t launch_f(const GemvParams& p, int64_t rows, int grid, cudaStream_t s
 
 namespace {
 std::atomic<int> g_static_weights{0};
+std::atomic<int64_t> g_tuning[kKnobCount] = {};
 }  // namespace
+
+int64_t tuning(int knob) {
+  return (knob >= 0 && knob < kKnobCount) ? g_tuning[knob].load(std::memory_order_relaxed) : 0;
+}
+bool set_tuning(int knob, int64_t value) {
+  if (knob < 0 || knob >= kKnobCount || value < 0) return false;
+  g_tuning[knob].store(value, std::memory_order_relaxed);
+  return true;
+}
 
 void set_static_weights(int on) { g_static_weights.store(on ? 1 : 0, std::memory_order_relaxed); }
 int static_weights() { return g_static_weights.load(std::memory_order_relaxed); }
 
 GemvPlan plan_gemv(Fmt f, int64_t M, int64_t N, int64_t K, int num_sms, int64_t batches) {
   GemvPlan pl;
+  pl.num_sms = num_sms;
   const int ck = (f == Fmt::I8R) ? 64 : 128;
   pl.spt = (int)((K + ck - 1) / ck);  // chunks a tile
   pl.tiles = (int)((N + kRows - 1) / kRows);
   // MXFP4: every tile is streamed once for each routed-expert batch
   const int64_t work = (int64_t)pl.tiles * pl.spt * std::max<int64_t>(1, batches);
   int64_t blocks = (int64_t)num_sms * kBlocksPerSM;
-  if (const char* env = std::getenv("WQ_GEMV_BLOCKS")) {  // tuning knob
-    const int v = std::atoi(env);
-    if (v >= 1) blocks = v;
-  }
+  if (const int64_t v = tuning(kKnobGemvBlocks); v >= 1) blocks = v;  // tuning and test knob
   blocks = std::min<int64_t>(blocks, (work + kWarps * kMinChunks - 1) / (kWarps * kMinChunks));
   pl.grid = (int)std::max<int64_t>(1, blocks);
   // equal chunk shares need a workspace and a single activation batch
@@ -1400,10 +1412,10 @@ cudaError_t launch_gemv(Fmt f, GemvParams p, const GemvPlan& pl, cudaStream_t st
   // MXFP4: the rows of one expert batch are gathered, at most R*S of them
   const int64_t rows = (f == Fmt::MXFP4) ? std::min<int64_t>(p.M * p.S, 16) : p.M;
   switch (f) {
-    case Fmt::I4G: return launch_f<Fmt::I4G>(p, rows, pl.grid, stream);
-    case Fmt::I4R: return launch_f<Fmt::I4R>(p, rows, pl.grid, stream);
-    case Fmt::I8R: return launch_f<Fmt::I8R>(p, rows, pl.grid, stream);
-    case Fmt::MXFP4: return launch_f<Fmt::MXFP4>(p, rows, pl.grid, stream);
+    case Fmt::I4G: return launch_f<Fmt::I4G>(p, rows, pl.grid, pl.num_sms, stream);
+    case Fmt::I4R: return launch_f<Fmt::I4R>(p, rows, pl.grid, pl.num_sms, stream);
+    case Fmt::I8R: return launch_f<Fmt::I8R>(p, rows, pl.grid, pl.num_sms, stream);
+    case Fmt::MXFP4: return launch_f<Fmt::MXFP4>(p, rows, pl.grid, pl.num_sms, stream);
   }
   return cudaErrorInvalidValue;
 }

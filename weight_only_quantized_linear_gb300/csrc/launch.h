@@ -35,6 +35,7 @@ struct GemvParams {
 };
 
 struct GemvPlan {
+  int num_sms = 152;      // SMs of the current device (queried)
   int grid = 1;           // thread blocks (a few an SM)
   int tiles = 1;          // 16-row weight tiles
   int spt = 1;            // 64-byte column chunks a tile
@@ -98,6 +99,22 @@ bool gemm_tc_supported(int64_t M, int64_t N, int64_t K, int32_t group);
 int gemm_tc_splits(int64_t M, int64_t N, int64_t K, int num_sms);
 size_t gemm_tc_ws_bytes(int64_t M, int64_t N, int64_t K, int num_sms);
 cudaError_t launch_gemm_tc(const GemmTcParams& p, int num_sms, cudaStream_t stream);
+
+// Tuning knobs (wq_set_tuning): set by an explicit call, read with one relaxed atomic
+// load where a launch is planned; 0 means the library's own choice.
+enum Knob { kKnobGemvBlocks = 0, kKnobGemvClusters, kKnobGemvPush, kKnobGemvXsmem, kKnobGemmMinM,
+            kKnobCount };
+int64_t tuning(int knob);
+bool set_tuning(int knob, int64_t value);
+
+// Probes (probe.cu): the bounded-wait failure path, and a pure HBM read stream.
+cudaError_t launch_wait_probe(uint64_t limit_ns, int arrive, int32_t* dev_status, cudaStream_t s);
+cudaError_t launch_stream_read(const void* buf, int64_t bytes, int variant, uint32_t* sink,
+                               int num_sms, cudaStream_t s);
+
+// A description of the last kernel launch the calling thread made (wq_last_launch).
+void note_launch(const char* fmt, ...);
+const char* last_launch();
 
 // Tensor-map encoding through the driver entry point (no link-time libcuda).
 bool encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, void* base,
