@@ -65,7 +65,8 @@ enum {
   WQ_DEV_NONFINITE = 1,   /* quantizer saw a non-finite weight or an overflowing range */
   WQ_DEV_BAD_EXPERT = 2,  /* an expert index outside [0, E); that slot's output is 0 */
   WQ_DEV_BAD_CODE = 4,    /* pack saw a code outside the 4-bit range; it packed code & 15 */
-  WQ_DEV_TIMEOUT = 8      /* a bounded device wait gave up (results invalid) */
+  WQ_DEV_TIMEOUT = 8,     /* a bounded device wait gave up (results invalid) */
+  WQ_DEV_BAD_ORDER = 16   /* an activation-order entry outside [0, K); that input read as 0 */
 };
 
 /* Quantizer modes for wq_quantize_groups. */
@@ -100,8 +101,15 @@ WQ_API const char* wq_last_launch(void);
  *                                byte k/2, unsigned 0..15)
  *   scale   f32  [N, K/G]
  *   zero    u8   [N, K/G]       (values 0..15)
- *   order   must be NULL (act-order input permutation is not implemented:
- *           WQ_EUNSUPPORTED otherwise)
+ *   order   i32 [K] or NULL: the activation order of a GPTQ checkpoint quantized in
+ *           activation order ([Linnet] Int4GroupLinear "optional order: [In; i32]";
+ *           "Importing GPTQ and AWQ": the layer gets an order and gathers its inputs
+ *           first).  Stored column j multiplies input order[j]:
+ *             y = x[:, order] . W-hat^T + bias
+ *           Entries must lie in [0, K) (repeats allowed); an entry outside reads as 0 and
+ *           sets WQ_DEV_BAD_ORDER.  The decode kernel gathers while it stages the
+ *           activations in shared memory; the other launches first gather x[:, order]
+ *           into the workspace (sized by wq_linear_int4_groups_ordered_workspace).
  *   bias    bf16 [N] or NULL
  *   y       bf16 [M, N]         (written; must not alias the inputs)
  *   group   G in {32, 64, 128, 256}; K % G == 0 (else WQ_ESHAPE)
@@ -123,9 +131,14 @@ WQ_API int wq_linear_int4_groups(const void* x, int64_t M, int64_t K,
                                  void* workspace, size_t ws_bytes, int32_t* dev_status,
                                  wq_stream_t stream);
 /* Workspace bytes wq_linear_int4_groups wants for (M, N, K, group) on the current
- * device (0 if the launch needs none). */
+ * device (0 if the launch needs none), with order == NULL. */
 WQ_API size_t wq_linear_int4_groups_workspace(int64_t M, int64_t N, int64_t K,
                                               int32_t group);
+/* The same with an activation order (order != NULL): room for the gathered activations
+ * x[:, order] (M * K bf16, rounded up to 256 bytes) ahead of the split-K scratch.  With
+ * order != NULL the workspace is required (WQ_EWORKSPACE if NULL or smaller than this). */
+WQ_API size_t wq_linear_int4_groups_ordered_workspace(int64_t M, int64_t N, int64_t K,
+                                                      int32_t group);
 
 /* ------------------------------------------------------------------------------------
  * Declare the weights immutable (the source pages have no counterpart: a launch-order
@@ -172,6 +185,7 @@ WQ_API int wq_set_static_weights(int on);
  * Results are those of wq_linear_int4_groups.
  * ------------------------------------------------------------------------------------ */
 #define WQ_NOALLOC_SCRATCH_BYTES (1024u * 1024u)
+/* (order must be NULL here: WQ_EUNSUPPORTED otherwise.) */
 WQ_API int wq_linear_int4_groups_noalloc(const void* x, int64_t M, int64_t K,
                                          const uint8_t* packed, const float* scale,
                                          const uint8_t* zero, const int32_t* order,
@@ -272,6 +286,53 @@ WQ_API int wq_mxfp4_experts_shared(const void* x, int64_t R, int64_t K,
                                    int32_t* dev_status, wq_stream_t stream);
 WQ_API size_t wq_mxfp4_experts_shared_workspace(int64_t R, int64_t S, int64_t E,
                                                 int64_t N, int64_t K);
+
+/* ------------------------------------------------------------------------------------
+ * [Linnet] mxfp4_linear_experts_shared(x, blocks, scales, experts): "std.nn.moe::
+ * linear_experts_shared with MXFP4 experts, many rows (x: [R, In])".  The product is
+ * that of wq_mxfp4_experts_shared, with x given as [R, K]:
+ *   y[r, s, n] = bf16( sum_k x[r, k] * W-hat_e[n, k] ),  e = experts[r, s]
+ * Arguments, layouts, limits and errors as wq_mxfp4_experts_shared.
+ * ------------------------------------------------------------------------------------ */
+WQ_API int wq_mxfp4_linear_experts_shared(const void* x, int64_t R, int64_t K,
+                                          const uint8_t* blocks, const uint8_t* scales,
+                                          int64_t E, int64_t N, const int32_t* experts,
+                                          int64_t S, void* y, void* workspace, size_t ws_bytes,
+                                          int32_t* dev_status, wq_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * [Linnet] mxfp4_experts(x, blocks, scales, experts): "a mixture's chosen experts
+ * multiplied from MXFP4, each slot its own input".
+ *   y[r, s, n] = bf16( sum_k x[r, s, k] * W-hat_e[n, k] ),  e = experts[r, s]
+ *   x bf16 [R, S, K] (one input row a slot); the other arguments as
+ *   wq_mxfp4_experts_shared (no workspace).  An expert index outside [0, E) gives a zero
+ *   slot and sets WQ_DEV_BAD_EXPERT.
+ * ------------------------------------------------------------------------------------ */
+WQ_API int wq_mxfp4_experts(const void* x, int64_t R, int64_t K, const uint8_t* blocks,
+                            const uint8_t* scales, int64_t E, int64_t N, const int32_t* experts,
+                            int64_t S, void* y, int32_t* dev_status, wq_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * [Linnet] mxfp4_combine_experts(x, blocks, scales, experts, weights): "std.nn.moe::
+ * combine_experts with MXFP4 experts".  The page gives the name and the arguments; the
+ * reading taken is the weighted sum of the row's routed experts over the shared input:
+ *   y[r, n] = bf16( sum_s weights[r, s] * sum_k x[r, k] * W-hat_e[n, k] ),  e = experts[r, s]
+ * a slot whose expert index lies outside [0, E) adding nothing (WQ_DEV_BAD_EXPERT set).
+ *   x bf16 [R, K] (or [R, 1, K]); weights f32 [R, S] (the combine weights, e.g. a softmax
+ *   over the row's routing logits); y bf16 [R, N].
+ *   workspace: R * S * N f32 slot results (wq_mxfp4_combine_experts_workspace), 16-byte
+ *   aligned, required (WQ_EINVAL if NULL, WQ_EWORKSPACE if too small); no zero-fill
+ *   needed.  Each slot's f32 result is multiplied by its weight in the product kernel's
+ *   epilogue; a second small kernel adds a row's slots in slot order (deterministic) and
+ *   rounds once to bf16.
+ * ------------------------------------------------------------------------------------ */
+WQ_API int wq_mxfp4_combine_experts(const void* x, int64_t R, int64_t K, const uint8_t* blocks,
+                                    const uint8_t* scales, int64_t E, int64_t N,
+                                    const int32_t* experts, int64_t S, const float* weights,
+                                    void* y, void* workspace, size_t ws_bytes,
+                                    int32_t* dev_status, wq_stream_t stream);
+WQ_API size_t wq_mxfp4_combine_experts_workspace(int64_t R, int64_t S, int64_t E, int64_t N,
+                                                 int64_t K);
 
 /* ------------------------------------------------------------------------------------
  * Round-to-nearest quantizer, ties to even, one scale per group of `group` consecutive

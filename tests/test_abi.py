@@ -50,9 +50,21 @@ def test_host_validation_without_a_device(lib):
     # null input
     assert lib.wq_linear_int4_groups(None, 1, 256, fake, fake, fake, None, None, 256, 128, fake, None, 0,
                                      None, None) == wq.WQ_EINVAL
-    # act-order permutation is not implemented
+    # an activation order needs room for the gathered activations in the workspace
     assert lib.wq_linear_int4_groups(fake, 1, 256, fake, fake, fake, fake, None, 256, 128, fake, None, 0,
-                                     None, None) == wq.WQ_EUNSUPPORTED
+                                     None, None) == wq.WQ_EWORKSPACE
+    assert lib.wq_linear_int4_groups_ordered_workspace(1, 256, 256, 128) >= 512
+    # ... and the allocation-free entry point has none
+    assert lib.wq_linear_int4_groups_noalloc(fake, 1, 256, fake, fake, fake, fake, None, 256, 128, fake,
+                                             None, None) == wq.WQ_EUNSUPPORTED
+    # the combine form needs its slot workspace
+    assert lib.wq_mxfp4_combine_experts(fake, 1, 64, fake, fake, 4, 8, fake, 2, fake, fake, None, 0, None,
+                                        None) == wq.WQ_EINVAL
+    assert lib.wq_mxfp4_combine_experts_workspace(3, 4, 32, 100, 64) == 3 * 4 * 100 * 4
+    # knobs: unknown knob or negative value
+    assert lib.wq_set_tuning(99, 1) == wq.WQ_EINVAL and lib.wq_set_tuning(0, -1) == wq.WQ_EINVAL
+    assert lib.wq_set_tuning(0, 0) == wq.WQ_OK
+    assert lib.wq_last_launch() is not None
     # group must divide K and be one of 32..256
     assert lib.wq_linear_int4_groups(fake, 1, 250, fake, fake, fake, None, None, 256, 128, fake, None, 0,
                                      None, None) == wq.WQ_ESHAPE

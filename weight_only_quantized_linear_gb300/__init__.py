@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libwq.so")
 HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "wq.h")
 
 WQ_OK, WQ_EINVAL, WQ_ESHAPE, WQ_EALIGN, WQ_ERANGE, WQ_EUNSUPPORTED, WQ_ECUDA, WQ_EWORKSPACE = range(8)
-WQ_DEV_NONFINITE, WQ_DEV_BAD_EXPERT, WQ_DEV_BAD_CODE, WQ_DEV_TIMEOUT = 1, 2, 4, 8
+WQ_DEV_NONFINITE, WQ_DEV_BAD_EXPERT, WQ_DEV_BAD_CODE, WQ_DEV_TIMEOUT, WQ_DEV_BAD_ORDER = 1, 2, 4, 8, 16
 WQ_SYM, WQ_SYM_U4, WQ_ASYM = 0, 1, 2
 (WQ_TUNE_GEMV_BLOCKS, WQ_TUNE_GEMV_CLUSTERS, WQ_TUNE_GEMV_PUSH, WQ_TUNE_GEMV_XSMEM,
  WQ_TUNE_GEMM_MIN_M) = range(5)
@@ -36,6 +36,7 @@ SIGNATURES = {
     "wq_linear_int4_groups": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P, _P, _P, _I64, _I32, _P, _P, _SZ,
                                              _P, _P]),
     "wq_linear_int4_groups_workspace": (_SZ, [_I64, _I64, _I64, _I32]),
+    "wq_linear_int4_groups_ordered_workspace": (_SZ, [_I64, _I64, _I64, _I32]),
     "wq_set_static_weights": (ctypes.c_int, [ctypes.c_int]),
     "wq_set_tuning": (ctypes.c_int, [_I32, _I64]),
     "wq_test_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, _I32, _P, _P]),
@@ -48,6 +49,12 @@ SIGNATURES = {
     "wq_mxfp4_experts_shared": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _I64, _P, _P, _SZ,
                                                _P, _P]),
     "wq_mxfp4_experts_shared_workspace": (_SZ, [_I64, _I64, _I64, _I64, _I64]),
+    "wq_mxfp4_linear_experts_shared": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _I64, _P, _P,
+                                                      _SZ, _P, _P]),
+    "wq_mxfp4_experts": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _I64, _P, _P, _P]),
+    "wq_mxfp4_combine_experts": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _I64, _P, _P, _P,
+                                                _SZ, _P, _P]),
+    "wq_mxfp4_combine_experts_workspace": (_SZ, [_I64, _I64, _I64, _I64, _I64]),
     "wq_quantize_groups": (ctypes.c_int, [_P, _I64, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _P]),
     "wq_pack_int4": (ctypes.c_int, [_P, _I64, _I64, _I32, _P, _P, _P]),
     "wq_unpack_int4": (ctypes.c_int, [_P, _I64, _I64, _I32, _P, _P]),
@@ -132,6 +139,10 @@ def wq_linear_int4_groups_workspace(M: int, N: int, K: int, group: int) -> int:
     return int(lib().wq_linear_int4_groups_workspace(M, N, K, group))
 
 
+def wq_linear_int4_groups_ordered_workspace(M: int, N: int, K: int, group: int) -> int:
+    return int(lib().wq_linear_int4_groups_ordered_workspace(M, N, K, group))
+
+
 def wq_linear_rows_workspace(M: int, N: int, K: int, bits: int) -> int:
     return int(lib().wq_linear_rows_workspace(M, N, K, bits))
 
@@ -185,6 +196,7 @@ def wq_linear_int4_groups(x, packed, scale, zero, bias=None, group=128, y=None, 
     _need(scale, torch.float32, "scale")
     _need(zero, torch.uint8, "zero")
     _need(bias, torch.bfloat16, "bias")
+    _need(order, torch.int32, "order", 1)
     M, K = x.shape
     N = packed.shape[0]
     if y is None:
@@ -269,6 +281,75 @@ def wq_mxfp4_experts_shared(x, blocks, scales, experts, y=None, workspace=None, 
                                        _ptr(y), _ptr(workspace), ws_bytes, _ptr(dev_status),
                                        _stream(stream))
     _check(st, "wq_mxfp4_experts_shared")
+    return y
+
+
+def wq_mxfp4_linear_experts_shared(x, blocks, scales, experts, y=None, workspace=None, dev_status=None,
+                                   stream=None):
+    """x bf16 [R, K]; blocks u8 [E, N, K/32, 16]; scales u8 [E, N, K/32]; experts i32
+    [R, S].  Returns y bf16 [R, S, N]."""
+    _need(x, torch.bfloat16, "x", 2)
+    _need(blocks, torch.uint8, "blocks", 4)
+    _need(scales, torch.uint8, "scales", 3)
+    _need(experts, torch.int32, "experts", 2)
+    R, K = x.shape
+    E, N = blocks.shape[0], blocks.shape[1]
+    S = experts.shape[1]
+    if y is None:
+        y = torch.empty((R, S, N), dtype=torch.bfloat16, device=x.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().wq_mxfp4_linear_experts_shared(_ptr(x), R, K, _ptr(blocks), _ptr(scales), E, N, _ptr(experts),
+                                              S, _ptr(y), _ptr(workspace), ws_bytes, _ptr(dev_status),
+                                              _stream(stream))
+    _check(st, "wq_mxfp4_linear_experts_shared")
+    return y
+
+
+def wq_mxfp4_experts(x, blocks, scales, experts, y=None, dev_status=None, stream=None):
+    """x bf16 [R, S, K] (one input a slot); blocks u8 [E, N, K/32, 16]; scales u8
+    [E, N, K/32]; experts i32 [R, S].  Returns y bf16 [R, S, N]."""
+    _need(x, torch.bfloat16, "x", 3)
+    _need(blocks, torch.uint8, "blocks", 4)
+    _need(scales, torch.uint8, "scales", 3)
+    _need(experts, torch.int32, "experts", 2)
+    R, S, K = x.shape
+    E, N = blocks.shape[0], blocks.shape[1]
+    if tuple(experts.shape) != (R, S):
+        raise ValueError("experts must be [R, S] with x [R, S, K]")
+    if y is None:
+        y = torch.empty((R, S, N), dtype=torch.bfloat16, device=x.device)
+    st = lib().wq_mxfp4_experts(_ptr(x), R, K, _ptr(blocks), _ptr(scales), E, N, _ptr(experts), S, _ptr(y),
+                                _ptr(dev_status), _stream(stream))
+    _check(st, "wq_mxfp4_experts")
+    return y
+
+
+def wq_mxfp4_combine_experts_workspace(R: int, S: int, E: int, N: int, K: int) -> int:
+    return int(lib().wq_mxfp4_combine_experts_workspace(R, S, E, N, K))
+
+
+def wq_mxfp4_combine_experts(x, blocks, scales, experts, weights, y=None, workspace=None, dev_status=None,
+                             stream=None):
+    """x bf16 [R, K] (or [R, 1, K]); experts i32 [R, S]; weights f32 [R, S].  Returns
+    y bf16 [R, N] = the rows' slot products weighted by `weights` and summed."""
+    _need(x, torch.bfloat16, "x")
+    _need(blocks, torch.uint8, "blocks", 4)
+    _need(scales, torch.uint8, "scales", 3)
+    _need(experts, torch.int32, "experts", 2)
+    _need(weights, torch.float32, "weights", 2)
+    R, K = x.shape[0], x.shape[-1]
+    E, N = blocks.shape[0], blocks.shape[1]
+    S = experts.shape[1]
+    if y is None:
+        y = torch.empty((R, N), dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(wq_mxfp4_combine_experts_workspace(R, S, E, N, K), dtype=torch.uint8,
+                                device=x.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib().wq_mxfp4_combine_experts(_ptr(x), R, K, _ptr(blocks), _ptr(scales), E, N, _ptr(experts), S,
+                                        _ptr(weights), _ptr(y), _ptr(workspace), ws_bytes, _ptr(dev_status),
+                                        _stream(stream))
+    _check(st, "wq_mxfp4_combine_experts")
     return y
 
 

@@ -170,20 +170,47 @@ WQ_API size_t wq_linear_int4_groups_workspace(int64_t M, int64_t N, int64_t K, i
   return gemv_ws_bytes(Fmt::I4G, M, N, K);
 }
 
+namespace {
+size_t gather_bytes(int64_t M, int64_t K) { return ((size_t)M * (size_t)K * 2 + 255) & ~size_t(255); }
+}  // namespace
+
+WQ_API size_t wq_linear_int4_groups_ordered_workspace(int64_t M, int64_t N, int64_t K,
+                                                      int32_t group) {
+  if (M <= 0 || N <= 0 || K <= 0 || group <= 0) return 0;
+  return gather_bytes(M, K) + wq_linear_int4_groups_workspace(M, N, K, group);
+}
+
 WQ_API int wq_linear_int4_groups(const void* x, int64_t M, int64_t K, const uint8_t* packed,
                                  const float* scale, const uint8_t* zero, const int32_t* order,
                                  const void* bias, int64_t N, int32_t group, void* y,
                                  void* workspace, size_t ws_bytes, int32_t* dev_status,
                                  wq_stream_t stream) {
-  if (order != nullptr) return WQ_EUNSUPPORTED;
   if (!zero) return WQ_EINVAL;
   int st = check_rows_common(x, M, K, packed, scale, bias, N, y);
   if (st != WQ_OK) return st;
   if (group != 32 && group != 64 && group != 128 && group != 256) return WQ_ESHAPE;
   if (K % group != 0) return WQ_ESHAPE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // activation order: the gathered copy of x takes the head of the workspace
+  __nv_bfloat16* xg = nullptr;
+  if (order != nullptr) {
+    const size_t gx = gather_bytes(M, K);
+    if (!aligned(order, 16)) return WQ_EALIGN;
+    if (workspace == nullptr || ws_bytes < gx) return WQ_EWORKSPACE;
+    if (!aligned(workspace, 256)) return WQ_EALIGN;
+    xg = static_cast<__nv_bfloat16*>(workspace);
+    workspace = static_cast<uint8_t*>(workspace) + gx;
+    ws_bytes -= gx;
+    if (ws_bytes == 0) workspace = nullptr;
+  }
 
   if (M > 16 && gemm_tc_supported(M, N, K, group)) {
+    if (order != nullptr) {
+      if (launch_gather_cols(static_cast<const __nv_bfloat16*>(x), order, M, K, xg, dev_status, s) !=
+          cudaSuccess)
+        return WQ_ECUDA;
+      x = xg;
+    }
     GemmTcParams gp{static_cast<const __nv_bfloat16*>(x), M, N, K, packed, scale, zero, group,
                     static_cast<const __nv_bfloat16*>(bias), static_cast<__nv_bfloat16*>(y),
                     dev_status, nullptr, 1};
@@ -211,6 +238,8 @@ WQ_API int wq_linear_int4_groups(const void* x, int64_t M, int64_t K, const uint
   p.bias = static_cast<const __nv_bfloat16*>(bias);
   p.y = static_cast<__nv_bfloat16*>(y);
   p.dev_status = dev_status;
+  p.order = order;
+  p.xg = xg;
   return run_gemv(Fmt::I4G, p, M <= 16 ? workspace : nullptr, ws_bytes, s);
 }
 
@@ -248,7 +277,7 @@ WQ_API int wq_linear_int4_groups_noalloc(const void* x, int64_t M, int64_t K,
                                          const uint8_t* zero, const int32_t* order,
                                          const void* bias, int64_t N, int32_t group, void* y,
                                          int32_t* dev_status, wq_stream_t stream) {
-  if (order != nullptr) return WQ_EUNSUPPORTED;
+  if (order != nullptr) return WQ_EUNSUPPORTED;  // the gathered copy of x needs a workspace
   if (!zero) return WQ_EINVAL;
   int st = check_rows_common(x, M, K, packed, scale, bias, N, y);
   if (st != WQ_OK) return st;
@@ -326,22 +355,12 @@ WQ_API size_t wq_mxfp4_experts_shared_workspace(int64_t R, int64_t S, int64_t E,
   return 0;
 }
 
-WQ_API int wq_mxfp4_experts_shared(const void* x, int64_t R, int64_t K, const uint8_t* blocks,
-                                   const uint8_t* scales, int64_t E, int64_t N,
-                                   const int32_t* experts, int64_t S, void* y, void* workspace,
-                                   size_t ws_bytes, int32_t* dev_status, wq_stream_t stream) {
-  (void)workspace; (void)ws_bytes;
-  if (!x || !blocks || !scales || !experts || !y) return WQ_EINVAL;
-  if (R <= 0 || K <= 0 || E <= 0 || N <= 0 || S <= 0) return WQ_EINVAL;
-  if (K % 32 != 0) return WQ_ESHAPE;
-  if (!gemv_mxfp4_supported(R, S, E) || E * N > (1 << 30)) return WQ_EUNSUPPORTED;
-  if (!aligned(x, 16) || !aligned(blocks, 16) || !aligned(experts, 4) || !aligned(y, 2))
-    return WQ_EALIGN;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // slots whose expert index is out of range are zero-filled by a small kernel
-  if (launch_zero_bad_slots(experts, R * S, E, N, static_cast<__nv_bfloat16*>(y), dev_status,
-                            s) != cudaSuccess)
-    return WQ_ECUDA;
+namespace {
+// The three MXFP4 expert products share one decode kernel: x_per_slot selects one input
+// row a slot; with y32 the slot results stay f32 (times sw) for the combine step.
+int run_mxfp4(const void* x, int64_t R, int64_t K, const uint8_t* blocks, const uint8_t* scales,
+              int64_t E, int64_t N, const int32_t* experts, int64_t S, void* y, float* y32,
+              const float* sw, int x_per_slot, int32_t* dev_status, cudaStream_t s) {
   GemvParams p{};
   p.x = static_cast<const __nv_bfloat16*>(x);
   p.w = blocks;
@@ -353,8 +372,89 @@ WQ_API int wq_mxfp4_experts_shared(const void* x, int64_t R, int64_t K, const ui
   p.S = S;
   p.E = E;
   p.y = static_cast<__nv_bfloat16*>(y);
+  p.y32 = y32;
+  p.sw = sw;
+  p.x_per_slot = x_per_slot;
   p.dev_status = dev_status;
   return run_gemv(Fmt::MXFP4, p, nullptr, 0, s);
+}
+
+int check_mxfp4(const void* x, int64_t R, int64_t K, const uint8_t* blocks, const uint8_t* scales,
+                int64_t E, int64_t N, const int32_t* experts, int64_t S, const void* y) {
+  if (!x || !blocks || !scales || !experts || !y) return WQ_EINVAL;
+  if (R <= 0 || K <= 0 || E <= 0 || N <= 0 || S <= 0) return WQ_EINVAL;
+  if (K % 32 != 0) return WQ_ESHAPE;
+  if (!gemv_mxfp4_supported(R, S, E) || E * N > (1 << 30)) return WQ_EUNSUPPORTED;
+  if (!aligned(x, 16) || !aligned(blocks, 16) || !aligned(experts, 4) || !aligned(y, 2))
+    return WQ_EALIGN;
+  return WQ_OK;
+}
+}  // namespace
+
+WQ_API int wq_mxfp4_experts_shared(const void* x, int64_t R, int64_t K, const uint8_t* blocks,
+                                   const uint8_t* scales, int64_t E, int64_t N,
+                                   const int32_t* experts, int64_t S, void* y, void* workspace,
+                                   size_t ws_bytes, int32_t* dev_status, wq_stream_t stream) {
+  (void)workspace; (void)ws_bytes;
+  int st = check_mxfp4(x, R, K, blocks, scales, E, N, experts, S, y);
+  if (st != WQ_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // slots whose expert index is out of range are zero-filled by a small kernel
+  if (launch_zero_bad_slots(experts, R * S, E, N, static_cast<__nv_bfloat16*>(y), dev_status,
+                            s) != cudaSuccess)
+    return WQ_ECUDA;
+  return run_mxfp4(x, R, K, blocks, scales, E, N, experts, S, y, nullptr, nullptr, 0, dev_status, s);
+}
+
+WQ_API int wq_mxfp4_linear_experts_shared(const void* x, int64_t R, int64_t K,
+                                          const uint8_t* blocks, const uint8_t* scales, int64_t E,
+                                          int64_t N, const int32_t* experts, int64_t S, void* y,
+                                          void* workspace, size_t ws_bytes, int32_t* dev_status,
+                                          wq_stream_t stream) {
+  return wq_mxfp4_experts_shared(x, R, K, blocks, scales, E, N, experts, S, y, workspace, ws_bytes,
+                                 dev_status, stream);
+}
+
+WQ_API int wq_mxfp4_experts(const void* x, int64_t R, int64_t K, const uint8_t* blocks,
+                            const uint8_t* scales, int64_t E, int64_t N, const int32_t* experts,
+                            int64_t S, void* y, int32_t* dev_status, wq_stream_t stream) {
+  int st = check_mxfp4(x, R, K, blocks, scales, E, N, experts, S, y);
+  if (st != WQ_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (launch_zero_bad_slots(experts, R * S, E, N, static_cast<__nv_bfloat16*>(y), dev_status,
+                            s) != cudaSuccess)
+    return WQ_ECUDA;
+  return run_mxfp4(x, R, K, blocks, scales, E, N, experts, S, y, nullptr, nullptr, 1, dev_status, s);
+}
+
+WQ_API size_t wq_mxfp4_combine_experts_workspace(int64_t R, int64_t S, int64_t E, int64_t N,
+                                                 int64_t K) {
+  (void)E; (void)K;
+  if (R <= 0 || S <= 0 || N <= 0) return 0;
+  return (size_t)R * (size_t)S * (size_t)N * 4;
+}
+
+WQ_API int wq_mxfp4_combine_experts(const void* x, int64_t R, int64_t K, const uint8_t* blocks,
+                                    const uint8_t* scales, int64_t E, int64_t N,
+                                    const int32_t* experts, int64_t S, const float* weights,
+                                    void* y, void* workspace, size_t ws_bytes,
+                                    int32_t* dev_status, wq_stream_t stream) {
+  int st = check_mxfp4(x, R, K, blocks, scales, E, N, experts, S, y);
+  if (st != WQ_OK) return st;
+  if (!weights || !workspace) return WQ_EINVAL;
+  if (ws_bytes < wq_mxfp4_combine_experts_workspace(R, S, E, N, K)) return WQ_EWORKSPACE;
+  if (!aligned(weights, 4) || !aligned(workspace, 16)) return WQ_EALIGN;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // bad slots only set the status bit: the combine step skips them
+  if (launch_zero_bad_slots(experts, R * S, E, N, nullptr, dev_status, s) != cudaSuccess)
+    return WQ_ECUDA;
+  float* y32 = static_cast<float*>(workspace);
+  st = run_mxfp4(x, R, K, blocks, scales, E, N, experts, S, nullptr, y32, weights, 0, dev_status, s);
+  if (st != WQ_OK) return st;
+  return launch_combine_slots(y32, experts, R, S, E, N, static_cast<__nv_bfloat16*>(y), s) ==
+                 cudaSuccess
+             ? WQ_OK
+             : WQ_ECUDA;
 }
 
 // ------------------------------------------------------------------ quantize / pack

@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM) k_gemv(const GemvParam
       if (m >= rt->pair_count[pr]) return -1;
       const int slot = rt->sorted[rt->pair_start[pr] + m];
       *yrow = slot;
-      return slot / (int)p.S;
+      return p.x_per_slot ? slot : slot / (int)p.S;
     } else {
       const int64_t row = (item / tiles) * kBatch + m;
       if (row >= p.M) return -1;
@@ -460,7 +460,10 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM) k_gemv(const GemvParam
               int yr = -1;
               if (xrow_of(item, m, &yr) >= 0 && n < N) {
                 if (p.bias) v += __bfloat162float(p.bias[n]);
-                p.y[(int64_t)yr * N + n] = __float2bfloat16_rn(v);
+                if (F == Fmt::MXFP4 && p.y32 != nullptr)
+                  p.y32[(int64_t)yr * N + n] = p.sw ? v * __ldg(p.sw + yr) : v;
+                else
+                  p.y[(int64_t)yr * N + n] = __float2bfloat16_rn(v);
               }
             } else if (m < p.M) {
               p.ws_part[((c * 2 + slot_id) * p.M + m) * kRows + row] = v;
@@ -807,14 +810,41 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     const uint32_t k8n = (uint32_t)(K / 8);
     const uint32_t xtotal = (uint32_t)M * k8n;
     const uint32_t xbase = smem_u32(xs);
+    bool bad_order = false;
     for (uint32_t base = 0; base < xtotal; base += 8 * kThreads) {
       uint4 v[8];
+      if (p.order == nullptr) {
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const uint32_t idx = base + q * kThreads + threadIdx.x;
-        if (idx < xtotal) {
-          const uint32_t m = idx / k8n, k8 = idx - m * k8n;
-          v[q] = ld_global_nc_v4(p.x + (int64_t)m * K + (int64_t)k8 * 8);
+        for (int q = 0; q < 8; ++q) {
+          const uint32_t idx = base + q * kThreads + threadIdx.x;
+          if (idx < xtotal) {
+            const uint32_t m = idx / k8n, k8 = idx - m * k8n;
+            v[q] = ld_global_nc_v4(p.x + (int64_t)m * K + (int64_t)k8 * 8);
+          }
+        }
+      } else {
+        // activation order: stored column j multiplies input order[j] ("Quantization"
+        // (Linnet docs), "Importing GPTQ and AWQ": the layer gathers its inputs first);
+        // an entry outside [0, K) reads as 0 and is reported
+        const unsigned short* xh = reinterpret_cast<const unsigned short*>(p.x);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint32_t idx = base + q * kThreads + threadIdx.x;
+          if (idx < xtotal) {
+            const uint32_t m = idx / k8n, k8 = idx - m * k8n;
+            const int4 o0 = __ldg(reinterpret_cast<const int4*>(p.order + (int64_t)k8 * 8));
+            const int4 o1 = __ldg(reinterpret_cast<const int4*>(p.order + (int64_t)k8 * 8 + 4));
+            const int oi[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
+            uint32_t h[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const bool ok = (uint32_t)oi[j] < (uint32_t)K;
+              bad_order |= !ok;
+              h[j] = ok ? (uint32_t)__ldg(xh + (int64_t)m * K + oi[j]) : 0u;
+            }
+            v[q] = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
+                              h[6] | (h[7] << 16));
+          }
         }
       }
 #pragma unroll
@@ -831,6 +861,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
         }
       }
     }
+    if (bad_order) set_dev_status(p.dev_status, WQ_DEV_BAD_ORDER);
     __syncthreads();
   }
 
@@ -1340,9 +1371,18 @@ cudaError_t launch_fact(const GemvParams& p, int num_sms, cudaStream_t stream) {
       return launch_fact_t<F, MT, 3, true, false>(p, maps, geo, ring3 + xbytes, clusters, num_sms, stream);
   }
   const FactGeom geo{0, cmax};
+  // activations read from global memory: an activation order is gathered first
+  GemvParams q = p;
+  if (q.order != nullptr) {
+    if (q.xg == nullptr) return cudaErrorInvalidValue;
+    const cudaError_t e = launch_gather_cols(q.x, q.order, q.M, q.K, q.xg, q.dev_status, stream);
+    if (e != cudaSuccess) return e;
+    q.x = q.xg;
+    q.order = nullptr;
+  }
   if (push_ok && fits(ring4 + recv))
-    return launch_fact_t<F, MT, 4, false, true>(p, maps, geo, ring4 + recv, clusters, num_sms, stream);
-  return launch_fact_t<F, MT, 4, false, false>(p, maps, geo, ring4, clusters, num_sms, stream);
+    return launch_fact_t<F, MT, 4, false, true>(q, maps, geo, ring4 + recv, clusters, num_sms, stream);
+  return launch_fact_t<F, MT, 4, false, false>(q, maps, geo, ring4, clusters, num_sms, stream);
 }
 
 // I4G with a group of at least 128 codes, I4R, I8R: the factored kernel (warp MMA,
@@ -1354,10 +1394,18 @@ cudaError_t launch_f(const GemvParams& p, int64_t rows, int grid, int num_sms, c
     if (fact_ok(F, p))
       return rows <= 8 ? launch_fact<F, 1>(p, num_sms, stream) : launch_fact<F, 2>(p, num_sms, stream);
   }
-  if (rows <= 1) return launch_t<F, 1, true>(p, grid, stream);
-  if (rows <= 2) return launch_t<F, 2, true>(p, grid, stream);
-  if (rows <= 8) return launch_t<F, 1, false>(p, grid, stream);
-  return launch_t<F, 2, false>(p, grid, stream);
+  GemvParams q = p;
+  if (q.order != nullptr) {  // the exact kernel reads activations from global memory
+    if (q.xg == nullptr) return cudaErrorInvalidValue;
+    const cudaError_t e = launch_gather_cols(q.x, q.order, q.M, q.K, q.xg, q.dev_status, stream);
+    if (e != cudaSuccess) return e;
+    q.x = q.xg;
+    q.order = nullptr;
+  }
+  if (rows <= 1) return launch_t<F, 1, true>(q, grid, stream);
+  if (rows <= 2) return launch_t<F, 2, true>(q, grid, stream);
+  if (rows <= 8) return launch_t<F, 1, false>(q, grid, stream);
+  return launch_t<F, 2, false>(q, grid, stream);
 }
 
 }  // namespace

@@ -28,6 +28,16 @@ struct GemvParams {
   int64_t E;               // MXFP4 experts
   const __nv_bfloat16* bias;
   __nv_bfloat16* y;        // [M, N] (MXFP4: [R * S, N])
+  // MXFP4 only: x holds one row a slot ([R * S, K], mxfp4_experts) instead of one a
+  // routed row ([R, K]); and, when y32 is set, every slot's f32 result times its weight
+  // sw[slot] (1 without sw) goes to y32 [R * S, N] instead of y (mxfp4_combine_experts)
+  int32_t x_per_slot;
+  float* y32;
+  const float* sw;
+  // I4G activation order (i32 [K]) or NULL; xg: scratch of M * K bf16 for the gathered
+  // activations of launches that do not gather while staging
+  const int32_t* order;
+  __nv_bfloat16* xg;
   float* ws_part;          // stream-K partial tiles [warps, 2, M, 16 rows]
   uint32_t* ws_cnt;        // stream-K arrival counters [tiles]
   int32_t* dev_status;
@@ -73,10 +83,19 @@ cudaError_t launch_dequant_i8r(const int8_t* q, const float* scale, int64_t N, i
                                void* w, cudaStream_t s);
 cudaError_t launch_dequant_i4r(const int8_t* packed, const float* scale, int64_t N, int64_t K,
                                void* w, cudaStream_t s);
+// Slots whose expert index is outside [0, E): their y rows are zeroed (y may be NULL:
+// only the status bit is set).
 cudaError_t launch_zero_bad_slots(const int32_t* experts, int64_t slots, int64_t E, int64_t N,
                                   __nv_bfloat16* y, int32_t* dev_status, cudaStream_t s);
+// y[r, n] = bf16(sum over slots s of row r, in slot order, of y32[r * S + s, n]); slots
+// with an expert index outside [0, E) add nothing.
+cudaError_t launch_combine_slots(const float* y32, const int32_t* experts, int64_t R, int64_t S,
+                                 int64_t E, int64_t N, __nv_bfloat16* y, cudaStream_t s);
 cudaError_t launch_dequant_mxfp4(const uint8_t* blocks, const uint8_t* scales, int64_t E,
                                  int64_t N, int64_t K, void* w, cudaStream_t s);
+// xg[m, j] = x[m, order[j]] (0 and WQ_DEV_BAD_ORDER for an entry outside [0, K)).
+cudaError_t launch_gather_cols(const __nv_bfloat16* x, const int32_t* order, int64_t M, int64_t K,
+                               __nv_bfloat16* xg, int32_t* dev_status, cudaStream_t s);
 
 // Large-M tensor-core GEMM (gemm_tc.cu).  Returns cudaErrorNotSupported when the shape
 // is outside what the kernel handles (the caller then uses the GEMV path).

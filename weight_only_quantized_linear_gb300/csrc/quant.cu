@@ -208,8 +208,47 @@ __global__ void k_zero_bad_slots(const int32_t* __restrict__ experts, int64_t sl
   const int32_t e = experts[slot];
   if (e >= 0 && e < E) return;
   if (threadIdx.x == 0) set_dev_status(dev_status, WQ_DEV_BAD_EXPERT);
+  if (y == nullptr) return;
   for (int64_t n = threadIdx.x; n < N; n += blockDim.x)
     y[slot * N + n] = __float2bfloat16_rn(0.0f);
+}
+
+// The combine step of mxfp4_combine_experts: the weighted slot results (f32, already
+// multiplied by their combine weights) of a row are added in slot order, then rounded
+// once to bf16.  Grid: (column chunks of 1024, rows).
+__global__ void __launch_bounds__(256) k_combine_slots(const float* __restrict__ y32,
+                                                       const int32_t* __restrict__ experts,
+                                                       int64_t S, int64_t E, int64_t N,
+                                                       __nv_bfloat16* __restrict__ y) {
+  const int64_t r = blockIdx.y;
+  const int64_t n = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (n >= N) return;
+  float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  for (int64_t s = 0; s < S; ++s) {
+    const int32_t e = __ldg(experts + r * S + s);
+    if (e < 0 || e >= E) continue;
+    const float* src = y32 + (r * S + s) * N + n;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (n + j < N) acc[j] += __ldcg(src + j);
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    if (n + j < N) y[r * N + n + j] = __float2bfloat16_rn(acc[j]);
+}
+
+// Activation order: xg[m, j] = x[m, order[j]] ("Quantization" (Linnet docs), "Importing
+// GPTQ and AWQ": the layer gathers its inputs first).
+__global__ void k_gather_cols(const unsigned short* __restrict__ x, const int32_t* __restrict__ order,
+                              int64_t M, int64_t K, unsigned short* __restrict__ xg,
+                              int32_t* dev_status) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= M * K) return;
+  const int64_t m = i / K, j = i - m * K;
+  const int32_t o = __ldg(order + j);
+  const bool ok = (uint32_t)o < (uint64_t)K;
+  xg[i] = ok ? __ldg(x + m * K + o) : (unsigned short)0;
+  if (!ok) set_dev_status(dev_status, WQ_DEV_BAD_ORDER);
 }
 
 inline unsigned blocks_for(int64_t n, int threads) {
@@ -268,6 +307,21 @@ cudaError_t launch_dequant_i4r(const int8_t* packed, const float* scale, int64_t
 cudaError_t launch_zero_bad_slots(const int32_t* experts, int64_t slots, int64_t E, int64_t N,
                                   __nv_bfloat16* y, int32_t* dev_status, cudaStream_t s) {
   k_zero_bad_slots<<<(unsigned)slots, 256, 0, s>>>(experts, slots, E, N, y, dev_status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_cols(const __nv_bfloat16* x, const int32_t* order, int64_t M, int64_t K,
+                               __nv_bfloat16* xg, int32_t* dev_status, cudaStream_t s) {
+  k_gather_cols<<<blocks_for(M * K, 256), 256, 0, s>>>(reinterpret_cast<const unsigned short*>(x), order,
+                                                      M, K, reinterpret_cast<unsigned short*>(xg),
+                                                      dev_status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_slots(const float* y32, const int32_t* experts, int64_t R, int64_t S,
+                                 int64_t E, int64_t N, __nv_bfloat16* y, cudaStream_t s) {
+  const dim3 grid((unsigned)((N + 1023) / 1024), (unsigned)R);
+  k_combine_slots<<<grid, 256, 0, s>>>(y32, experts, S, E, N, y);
   return cudaGetLastError();
 }
 
