@@ -265,6 +265,30 @@ def run_prefill(dev, weights, layers, peaks, stream):
         us = time_rotating(call, reps, stream)
         sweep[str(M)] = {"us": round(us, 2), "gbs": round(proj_bytes(N, K, M) / (us * 1e-6) / 1e9, 1),
                          "tflops": round(2.0 * M * N * K / us / 1e6, 2), "kernel": wq.wq_last_launch()}
+    # the regime crossover: the decode kernels and the tensor-core GEMM at M = 17 .. 128
+    cross = {}
+    for M in (17, 24, 32, 48, 64, 96, 128):
+        xm = [x[:M].contiguous() for x in xs[K]]
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        row = {}
+        for regime, min_m in (("decode", 100000), ("tcgen05", 1)):
+            wq.wq_set_tuning(wq.WQ_TUNE_GEMM_MIN_M, min_m)
+            try:
+                wsb = wq.wq_linear_int4_groups_workspace(M, N, K, GROUP)
+                ws = [wq.alloc_workspace(wsb, dev) for _ in range(layers)] if wsb else [None] * layers
+
+                def call(i, M=M, xm=xm, y=y, ws=ws):
+                    p_, s_, z_ = weights[i % layers]["gate"]
+                    wq.wq_linear_int4_groups(xm[i % len(xm)], p_, s_, z_, None, GROUP, y=y, workspace=ws[i % layers],
+                                             stream=stream)
+
+                us = time_rotating(call, reps, stream)
+                row[regime] = {"us": round(us, 2), "kernel": wq.wq_last_launch()}
+            finally:
+                wq.wq_set_tuning(wq.WQ_TUNE_GEMM_MIN_M, 0)
+        row["faster"] = min(("decode", "tcgen05"), key=lambda r: row[r]["us"])
+        cross[str(M)] = row
+    sweep["crossover_gate_14336x4096"] = cross
     return prefill, sweep
 
 
@@ -468,6 +492,70 @@ def run_stream_ceiling(dev, peaks, stream, reps: int = 20):
     return out
 
 
+def run_prepared_decode(dev, weights, layers, xs, stream, steps, warmup, row_major_per_kind):
+    """The decode step on the prepared layout (wq_prepare_int4_groups at load time, outside
+    the timed region; wq_linear_int4_groups_prepared in the step): the same 7 projections
+    x 32 layers, the same algorithmic bytes, against the row-major layout's step."""
+    import torch
+
+    import weight_only_quantized_linear_gb300 as wq
+    from weight_only_quantized_linear_gb300 import synth
+
+    names = synth.LLAMA_ORDER
+    prep = [{n: wq.wq_prepare_int4_groups(*weights[l][n], GROUP) for n in names} for l in range(layers)]
+    torch.cuda.synchronize()
+    ys = {(l, n): torch.empty((1, synth.LLAMA_PROJ[n][0]), dtype=torch.bfloat16, device=dev)
+          for l in range(layers) for n in names}
+    ws = {n: [wq.alloc_workspace(wq.wq_linear_int4_groups_prepared_workspace(1, *synth.LLAMA_PROJ[n], GROUP), dev)
+              for _ in range(layers)] for n in names}
+    launched = {}
+
+    def launch_kind(n):
+        N, K = synth.LLAMA_PROJ[n]
+        for l in range(layers):
+            wq.wq_linear_int4_groups_prepared(xs[K], prep[l][n], N, None, GROUP, y=ys[(l, n)], workspace=ws[n][l],
+                                              stream=stream)
+
+    with torch.cuda.stream(stream):
+        for n in names:
+            launch_kind(n)
+            launched[n] = wq.wq_last_launch()
+    torch.cuda.synchronize()
+    graphs = {}
+    for n in names:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            launch_kind(n)
+        graphs[n] = g
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            for n in names:
+                graphs[n].replay()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for st in range(steps):
+            for i, n in enumerate(names):
+                evs[st][i].record(stream)
+                graphs[n].replay()
+            evs[st][len(names)].record(stream)
+        t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    step_bytes = sum(proj_bytes(*synth.LLAMA_PROJ[n]) for n in names) * layers
+    per = {}
+    for i, n in enumerate(names):
+        us = sum(e[i].elapsed_time(e[i + 1]) for e in evs) / (steps * layers) * 1e3
+        per[n] = {"us_per_launch": round(us, 3), "gbs": round(proj_bytes(*synth.LLAMA_PROJ[n]) / (us * 1e-6) / 1e9, 1),
+                  "row_major_us": row_major_per_kind[n]["us_per_launch"], "kernel": launched[n]}
+    del prep, graphs
+    return {"value": round(step_bytes / (ms * 1e-3) / 1e9, 1), "unit": UNIT, "ms_per_step": round(ms, 4),
+            "per_projection": per,
+            "how": "weights repacked once at load (wq_prepare_int4_groups, not timed); same bytes, same step"}
+
+
 def build_weights(dev, layers: int, seed0: int = 1000):
     """Per layer and projection: packed u8 [N, K/2], scale f32 [N, K/G], zero u8 [N, K/G]."""
     import torch
@@ -584,6 +672,10 @@ def run_gpu(args):
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
+    per_kind_pre = {}
+    for i, n in enumerate(names):
+        us = sum(evs[i].elapsed_time(evs[i + 1]) for evs in step_events) / (args.steps * layers) * 1e3
+        per_kind_pre[n] = {"us_per_launch": round(us, 3)}
 
     # ---------------- the other legs: fused decode step, M = 2048, M sweep, variants ----------------
     prefill = sweep = rows_leg = mxfp4_leg = None
@@ -591,6 +683,8 @@ def run_gpu(args):
     clocks_p.start()
     ceiling = run_stream_ceiling(dev, peaks, stream)
     fused_leg = run_fused_decode(dev, weights, layers, xs, stream, max(10, min(args.steps, 500)), args.warmup)
+    prepared_leg = run_prepared_decode(dev, weights, layers, xs, stream, max(10, min(args.steps, 500)), args.warmup,
+                                       per_kind_pre)
     if not args.no_prefill:
         prefill, sweep = run_prefill(dev, weights, layers, peaks, stream)
         rows_leg, mxfp4_leg = run_variants(dev, peaks, stream)
@@ -705,6 +799,7 @@ def run_gpu(args):
             "cpu_baseline": cpu,
             "prefill_m2048": prefill,
             "decode_fused_qkv_gateup": fused_leg,
+            "decode_prepared_layout": prepared_leg,
             "m_sweep_gate": sweep,
             "rows_int8_int4": rows_leg,
             "mxfp4_experts_shared": mxfp4_leg,

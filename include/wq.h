@@ -141,6 +141,43 @@ WQ_API size_t wq_linear_int4_groups_ordered_workspace(int64_t M, int64_t N, int6
                                                       int32_t group);
 
 /* ------------------------------------------------------------------------------------
+ * Prepared group-wise 4-bit weights: [Linnet] "Group-wise 4-bit weights" (weights
+ * repacked at load, --prepare); [Ch20] "Speed needs a kernel" (weight layouts pre-shuffled
+ * so that a 128-bit load fills a tensor-core fragment directly).
+ *
+ * wq_prepare_int4_groups copies an Int4GroupLinear layer (packed [N, K/2], scale and
+ * zero [N, K/G], as for wq_linear_int4_groups) into one device buffer of
+ * wq_prepared_int4_groups_bytes(N, K, group) bytes in the order the decode kernel
+ * consumes it: for every block of 128 rows and every 256 codes, 16384 bytes of codes
+ * (fragment-ordered, bank-swizzled, nibbles in pair order) followed by the 128 rows' two
+ * scales and two zero points (1280 bytes); rows past N are padded with code 0, scale 0.
+ * Same bytes a weight as the public layout (plus the row padding).  A load-time step:
+ * asynchronous on `stream`, bit-exact (codes, scales and zero points are only moved).
+ * Requires K % 256 == 0 and a power-of-two group of 128 or more (else
+ * wq_prepared_int4_groups_bytes returns 0 and the call WQ_EUNSUPPORTED); prepared 16-byte
+ * aligned; prepared_bytes too small: WQ_EWORKSPACE.
+ *
+ * wq_linear_int4_groups_prepared computes the product of wq_linear_int4_groups (the same
+ * definition, result and tolerance) from the prepared copy, for the decode regime:
+ * M <= 16 (WQ_EUNSUPPORTED above; the prefill regime reads the public layout).  No
+ * activation order.  workspace: as wq_linear_int4_groups, sized by
+ * wq_linear_int4_groups_prepared_workspace(); NULL runs whole 128-row blocks a thread
+ * block.  Each step of the kernel arrives with two bulk copies of the prepared bytes and
+ * one 512-byte copy of each activation row.
+ * ------------------------------------------------------------------------------------ */
+WQ_API size_t wq_prepared_int4_groups_bytes(int64_t N, int64_t K, int32_t group);
+WQ_API int wq_prepare_int4_groups(const uint8_t* packed, const float* scale, const uint8_t* zero,
+                                  int64_t N, int64_t K, int32_t group, void* prepared,
+                                  size_t prepared_bytes, wq_stream_t stream);
+WQ_API int wq_linear_int4_groups_prepared(const void* x, int64_t M, int64_t K,
+                                          const void* prepared, const void* bias, int64_t N,
+                                          int32_t group, void* y, void* workspace,
+                                          size_t ws_bytes, int32_t* dev_status,
+                                          wq_stream_t stream);
+WQ_API size_t wq_linear_int4_groups_prepared_workspace(int64_t M, int64_t N, int64_t K,
+                                                       int32_t group);
+
+/* ------------------------------------------------------------------------------------
  * Declare the weights immutable (the source pages have no counterpart: a launch-order
  * promise made by the caller, not an operation of the method).
  *
@@ -201,14 +238,23 @@ WQ_API int wq_linear_int4_groups_noalloc(const void* x, int64_t M, int64_t K,
  *   WQ_TUNE_GEMV_CLUSTERS  thread-block clusters of the factored decode kernel
  *   WQ_TUNE_GEMV_PUSH      cut-tile fixup of the factored kernel: 1 push, 2 cluster barriers
  *   WQ_TUNE_GEMV_XSMEM     1: never stage activations in shared memory
- *   WQ_TUNE_GEMM_MIN_M     smallest M that takes the tensor-core GEMM (default 32)
+ *   WQ_TUNE_GEMM_MIN_M     smallest M that takes the tensor-core GEMM (default 40)
+ *   WQ_TUNE_DECODE         decode kernel for the affine formats: 0 (and 1) the cluster
+ *                          kernel, 2 the exact kernel
+ *   WQ_TUNE_PREP           prepared-layout kernel launch, bit mask: 1 without programmatic
+ *                          dependent launch, 2 without streaming weights before the
+ *                          dependency wait
+ *   WQ_TUNE_PREP_BLOCKS_PER_SM  blocks an SM the prepared-layout kernel is sized for (2)
  * ------------------------------------------------------------------------------------ */
 enum {
   WQ_TUNE_GEMV_BLOCKS = 0,
   WQ_TUNE_GEMV_CLUSTERS = 1,
   WQ_TUNE_GEMV_PUSH = 2,
   WQ_TUNE_GEMV_XSMEM = 3,
-  WQ_TUNE_GEMM_MIN_M = 4
+  WQ_TUNE_GEMM_MIN_M = 4,
+  WQ_TUNE_DECODE = 5,
+  WQ_TUNE_PREP = 6,
+  WQ_TUNE_PREP_BLOCKS_PER_SM = 7
 };
 WQ_API int wq_set_tuning(int32_t knob, int64_t value);
 

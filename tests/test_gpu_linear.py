@@ -435,3 +435,22 @@ def test_factored_cut_tile_fixup(cuda_device, tune, mode, M, N, K, clusters):
     assert_within(y[:, torch.from_numpy(rows).to(d)], yr, ad, f"{mode} M={M} N={N} K={K}")
     y2 = run_i4g(d, *args)
     assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+
+
+def test_one_workspace_shared_by_shapes_in_turn(cuda_device):
+    """Calls of different shapes and kernels that share one workspace in turn (never
+    concurrently) all stay correct: every call leaves the whole workspace zero-filled."""
+    d = cuda_device
+    shapes = [(2, 300, 2048, 64), (1, 4096, 4096, 128), (5, 1000, 6144, 128), (1, 300, 2048, 64),
+              (13, 4096, 4096, 128), (1, 1000, 4096 + 1024, 128), (64, 256, 4096, 128)]
+    need = max(wq.wq_linear_int4_groups_workspace(M, N, K, G) for M, N, K, G in shapes)
+    ws = torch.zeros(need, dtype=torch.uint8, device=d)
+    for i, (M, N, K, G) in enumerate(shapes):
+        packed, scale, zero = make_i4g(N, K, G, seed=i)
+        x = synth.normal_bf16((M, K), seed=i + 50)
+        y = wq.wq_linear_int4_groups(dev(x, d), dev(packed, d), dev(scale, d), dev(zero, d), None, G, workspace=ws)
+        torch.cuda.synchronize()
+        assert int(ws.view(torch.int32).abs().sum().item()) == 0, f"workspace dirty after {M, N, K, G}"
+        rows = np.random.default_rng(i).choice(N, min(N, 128), replace=False)
+        yr, ad = oracle.linear_int4_groups(bf16_bits(x), packed[rows], scale[rows], zero[rows], None, len(rows), G)
+        assert_within(y[:, torch.from_numpy(rows).to(d)], yr, ad, f"shared workspace {M, N, K, G}")

@@ -22,7 +22,7 @@ WQ_OK, WQ_EINVAL, WQ_ESHAPE, WQ_EALIGN, WQ_ERANGE, WQ_EUNSUPPORTED, WQ_ECUDA, WQ
 WQ_DEV_NONFINITE, WQ_DEV_BAD_EXPERT, WQ_DEV_BAD_CODE, WQ_DEV_TIMEOUT, WQ_DEV_BAD_ORDER = 1, 2, 4, 8, 16
 WQ_SYM, WQ_SYM_U4, WQ_ASYM = 0, 1, 2
 (WQ_TUNE_GEMV_BLOCKS, WQ_TUNE_GEMV_CLUSTERS, WQ_TUNE_GEMV_PUSH, WQ_TUNE_GEMV_XSMEM,
- WQ_TUNE_GEMM_MIN_M) = range(5)
+ WQ_TUNE_GEMM_MIN_M, WQ_TUNE_DECODE, WQ_TUNE_PREP, WQ_TUNE_PREP_BLOCKS_PER_SM) = range(8)
 
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
@@ -37,6 +37,11 @@ SIGNATURES = {
                                              _P, _P]),
     "wq_linear_int4_groups_workspace": (_SZ, [_I64, _I64, _I64, _I32]),
     "wq_linear_int4_groups_ordered_workspace": (_SZ, [_I64, _I64, _I64, _I32]),
+    "wq_prepared_int4_groups_bytes": (_SZ, [_I64, _I64, _I32]),
+    "wq_prepare_int4_groups": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _I32, _P, _SZ, _P]),
+    "wq_linear_int4_groups_prepared": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _I64, _I32, _P, _P, _SZ, _P,
+                                                      _P]),
+    "wq_linear_int4_groups_prepared_workspace": (_SZ, [_I64, _I64, _I64, _I32]),
     "wq_set_static_weights": (ctypes.c_int, [ctypes.c_int]),
     "wq_set_tuning": (ctypes.c_int, [_I32, _I64]),
     "wq_test_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, _I32, _P, _P]),
@@ -206,6 +211,43 @@ def wq_linear_int4_groups(x, packed, scale, zero, bias=None, group=128, y=None, 
                                      _ptr(bias), N, group, _ptr(y), _ptr(workspace), ws_bytes,
                                      _ptr(dev_status), _stream(stream))
     _check(st, "wq_linear_int4_groups")
+    return y
+
+
+def wq_prepare_int4_groups(packed, scale, zero, group=128, stream=None):
+    """The load-time repack of an Int4GroupLinear layer (see wq.h): returns the prepared
+    u8 buffer the decode kernel streams."""
+    _need(packed, torch.uint8, "packed")
+    _need(scale, torch.float32, "scale")
+    _need(zero, torch.uint8, "zero")
+    N = packed.shape[0]
+    K = scale.shape[1] * group
+    nbytes = int(lib().wq_prepared_int4_groups_bytes(N, K, group))
+    if nbytes == 0:
+        raise WQError(WQ_EUNSUPPORTED, "wq_prepare_int4_groups")
+    out = torch.empty(nbytes, dtype=torch.uint8, device=packed.device)
+    _check(lib().wq_prepare_int4_groups(_ptr(packed), _ptr(scale), _ptr(zero), N, K, group, _ptr(out), nbytes,
+                                        _stream(stream)), "wq_prepare_int4_groups")
+    return out
+
+
+def wq_linear_int4_groups_prepared_workspace(M: int, N: int, K: int, group: int) -> int:
+    return int(lib().wq_linear_int4_groups_prepared_workspace(M, N, K, group))
+
+
+def wq_linear_int4_groups_prepared(x, prepared, N, bias=None, group=128, y=None, workspace=None, dev_status=None,
+                                   stream=None):
+    """y = x . W-hat^T (+ bias) from the prepared copy of the layer (decode regime, M <= 16)."""
+    _need(x, torch.bfloat16, "x", 2)
+    _need(prepared, torch.uint8, "prepared")
+    _need(bias, torch.bfloat16, "bias")
+    M, K = x.shape
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().wq_linear_int4_groups_prepared(_ptr(x), M, K, _ptr(prepared), _ptr(bias), N, group, _ptr(y),
+                                              _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream))
+    _check(st, "wq_linear_int4_groups_prepared")
     return y
 
 

@@ -6,6 +6,7 @@
 // synchronizes, allocates device memory or throws.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <mutex>
@@ -69,7 +70,8 @@ int run_gemv(Fmt f, GemvParams p, void* workspace, size_t ws_bytes, cudaStream_t
   return launch_gemv(f, p, pl, stream) == cudaSuccess ? WQ_OK : WQ_ECUDA;
 }
 
-size_t gemv_ws_bytes(Fmt f, int64_t M, int64_t N, int64_t K) {
+size_t gemv_ws_bytes(Fmt f, int64_t M, int64_t N, int64_t K, int32_t group) {
+  (void)group;
   return plan_gemv(f, M, N, K, num_sms_current()).ws_bytes;
 }
 
@@ -167,7 +169,7 @@ WQ_API size_t wq_linear_int4_groups_workspace(int64_t M, int64_t N, int64_t K, i
   if (M <= 0 || N <= 0 || K <= 0 || group <= 0) return 0;
   if (M > 16 && gemm_tc_supported(M, N, K, group)) return gemm_tc_ws_bytes(M, N, K, num_sms_current());
   if (M > 16) return 0;
-  return gemv_ws_bytes(Fmt::I4G, M, N, K);
+  return gemv_ws_bytes(Fmt::I4G, M, N, K, group);
 }
 
 namespace {
@@ -243,6 +245,57 @@ WQ_API int wq_linear_int4_groups(const void* x, int64_t M, int64_t K, const uint
   return run_gemv(Fmt::I4G, p, M <= 16 ? workspace : nullptr, ws_bytes, s);
 }
 
+// ------------------------------------------------------------------ prepared layout
+WQ_API size_t wq_prepared_int4_groups_bytes(int64_t N, int64_t K, int32_t group) {
+  if (!prep_shape_ok(1, N, K, group)) return 0;
+  return prep_bytes(N, K);
+}
+
+WQ_API int wq_prepare_int4_groups(const uint8_t* packed, const float* scale, const uint8_t* zero,
+                                  int64_t N, int64_t K, int32_t group, void* prepared,
+                                  size_t prepared_bytes, wq_stream_t stream) {
+  if (!packed || !scale || !zero || !prepared) return WQ_EINVAL;
+  if (N <= 0 || K <= 0 || group <= 0) return WQ_EINVAL;
+  if (!prep_shape_ok(1, N, K, group)) return WQ_EUNSUPPORTED;
+  if (prepared_bytes < prep_bytes(N, K)) return WQ_EWORKSPACE;
+  if (!aligned(packed, 4) || !aligned(scale, 4) || !aligned(prepared, 16)) return WQ_EALIGN;
+  return launch_prepare(packed, scale, zero, N, K, group, static_cast<uint8_t*>(prepared),
+                        reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? WQ_OK
+             : WQ_ECUDA;
+}
+
+WQ_API size_t wq_linear_int4_groups_prepared_workspace(int64_t M, int64_t N, int64_t K,
+                                                       int32_t group) {
+  if (!prep_shape_ok(M, N, K, group)) return 0;
+  return prep_ws_bytes(M, N, K, num_sms_current());
+}
+
+WQ_API int wq_linear_int4_groups_prepared(const void* x, int64_t M, int64_t K, const void* prepared,
+                                          const void* bias, int64_t N, int32_t group, void* y,
+                                          void* workspace, size_t ws_bytes, int32_t* dev_status,
+                                          wq_stream_t stream) {
+  if (!x || !prepared || !y) return WQ_EINVAL;
+  if (M <= 0 || N <= 0 || K <= 0 || group <= 0) return WQ_EINVAL;
+  if (!prep_shape_ok(M, N, K, group)) return M > 16 ? WQ_EUNSUPPORTED : WQ_ESHAPE;
+  if (!aligned(x, 16) || !aligned(prepared, 16) || !aligned(y, 2) || (bias && !aligned(bias, 2)))
+    return WQ_EALIGN;
+  GemvParams p{};
+  p.x = static_cast<const __nv_bfloat16*>(x);
+  p.M = M;
+  p.K = K;
+  p.N = N;
+  p.group = group;
+  p.group_shift = __builtin_ctz((unsigned)group);
+  p.bias = static_cast<const __nv_bfloat16*>(bias);
+  p.y = static_cast<__nv_bfloat16*>(y);
+  p.dev_status = dev_status;
+  return launch_prep(p, static_cast<const uint8_t*>(prepared), workspace, ws_bytes, num_sms_current(),
+                     reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? WQ_OK
+             : WQ_ECUDA;
+}
+
 // ------------------------------------------------------------------ allocation-free variant
 // Scratch for callers that cannot allocate device memory (see wq.h): one static array a
 // GPU, its device address looked up once per device with cudaGetSymbolAddress (the
@@ -303,7 +356,7 @@ WQ_API int wq_linear_int4_groups_noalloc(const void* x, int64_t M, int64_t K,
 // ------------------------------------------------------------------ per-row int8 / int4
 WQ_API size_t wq_linear_rows_workspace(int64_t M, int64_t N, int64_t K, int32_t bits) {
   if (M <= 0 || N <= 0 || K <= 0 || M > 16) return 0;
-  return gemv_ws_bytes(bits == 8 ? Fmt::I8R : Fmt::I4R, M, N, K);
+  return gemv_ws_bytes(bits == 8 ? Fmt::I8R : Fmt::I4R, M, N, K, 0);
 }
 
 WQ_API int wq_linear_int8_rows(const void* x, int64_t M, int64_t K, const int8_t* q,

@@ -209,6 +209,16 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
                : "r"(addr));
   return v;
 }
+__device__ __forceinline__ float2 ld_shared_f32x2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_shared_u16(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
 __device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
   float v;
   asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
@@ -410,6 +420,43 @@ __device__ __forceinline__ void dequant_e2m1x8(uint32_t w, float2 X, uint32_t (&
     out[i] = pack_bf16x2(v.x, v.y);
   }
 }
+
+// ------------------------------------------------------------------ factored decode helpers
+// The factored decode kernels form (q - zero) exactly in bf16 and multiply the chunk's
+// f32 sum by its scale once (the definition's products reassociated, see gemv.cu).
+// Four int8 codes of a word as exact bf16x2 pairs (k0, k1) and (k2, k3).
+__device__ __forceinline__ void i8x4_to_bf16x2(uint32_t w, uint32_t (&out)[2]) {
+  const uint32_t u = w ^ 0x80808080u;                      // bytes q + 128
+  const float2 c = make_float2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
+  const float2 f01 =
+      __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440)),
+                             __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441))), c);
+  const float2 f23 =
+      __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7442)),
+                             __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443))), c);
+  out[0] = pack_bf16x2(f01.x, f01.y);
+  out[1] = pack_bf16x2(f23.x, f23.y);
+}
+
+// Eight 4-bit codes of a word (even element in the low nibble) minus a zero point, as
+// exact bf16x2 pairs d[j] = (k j, k j + 4).  zc = bf16x2 of 128 + min(z, 127); zc2 = bf16x2
+// of max(z - 127, 0), used only when `big`; magic = 0x43004300 (bf16x2 128, 128) held in a
+// register.
+template <bool kBig>
+__device__ __forceinline__ void nib8_minus_zero(uint32_t w, uint32_t zc, uint32_t zc2,
+                                                uint32_t magic, uint32_t (&d)[4]) {
+  // plain shifts (measured faster on sm_103a than high halves of products, which move
+  // them to the FMA pipe)
+  d[0] = sub_bf16x2(and_0f_or(w, magic), zc);
+  d[1] = sub_bf16x2(and_0f_or(w >> 4, magic), zc);
+  d[2] = sub_bf16x2(and_0f_or(w >> 8, magic), zc);
+  d[3] = sub_bf16x2(and_0f_or(w >> 12, magic), zc);
+  if constexpr (kBig) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) d[j] = sub_bf16x2(d[j], zc2);
+  }
+}
+
 
 __device__ __forceinline__ void set_dev_status(int32_t* st, int32_t bits) {
   if (st) atomicOr(st, bits);

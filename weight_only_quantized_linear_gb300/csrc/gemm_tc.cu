@@ -471,8 +471,11 @@ size_t gemm_tc_ws_bytes(int64_t M, int64_t N, int64_t K, int num_sms) {
 }
 
 bool gemm_tc_supported(int64_t M, int64_t N, int64_t K, int32_t group) {
+  // The crossover, measured on GB300 on the 14336 x 4096 group-128 layer: the decode
+  // kernel and this GEMM tie at M = 17 .. 32 (40 us either way), the GEMM is faster from
+  // M = 48 on (45 us against 57 us); the default switches in between.
   const int64_t min_m = tuning(kKnobGemmMinM);  // tuning and test knob for the crossover
-  if (M < (min_m >= 1 ? min_m : 32)) return false;
+  if (M < (min_m >= 1 ? min_m : 40)) return false;
   return N >= 1 && K >= 32 && K % 32 == 0 && (group == 32 || group == 64 || group == 128 ||
                                                group == 256) &&
          K % group == 0 && M <= (int64_t(1) << 31) && N <= (int64_t(1) << 31);

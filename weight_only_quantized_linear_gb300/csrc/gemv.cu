@@ -119,8 +119,11 @@ __device__ __forceinline__ void finish_cut_tiles(const GemvParams& p, int64_t c,
             if (cc <= c1) {
               const int64_t b0 = bound(cc);
               if (b0 != bound(cc + 1)) {
+                // read, then cleared: the call leaves the workspace zero-filled
                 const int sid = (b0 >= t_beg) ? 0 : 1;
-                part[q] = __ldcg(&p.ws_part[((cc * 2 + sid) * p.M + m) * kRows + row]);
+                float* src = &p.ws_part[((cc * 2 + sid) * p.M + m) * kRows + row];
+                part[q] = __ldcg(src);
+                __stcg(src, 0.0f);
               }
             }
           }
@@ -548,42 +551,6 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM) k_gemv(const GemvParam
 // MMA is a permutation shared by A and B: the nibble extraction yields the pairs
 // (k, k + 4) of a word, so each lane permutes its activations into the same pairs once a
 // chunk (shared by both rows and every MMA of the chunk).
-namespace {
-
-// Four int8 codes of a word as exact bf16x2 pairs (k0, k1) and (k2, k3).
-__device__ __forceinline__ void i8x4_to_bf16x2(uint32_t w, uint32_t (&out)[2]) {
-  const uint32_t u = w ^ 0x80808080u;                      // bytes q + 128
-  const float2 c = make_float2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
-  const float2 f01 =
-      __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440)),
-                             __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441))), c);
-  const float2 f23 =
-      __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7442)),
-                             __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443))), c);
-  out[0] = pack_bf16x2(f01.x, f01.y);
-  out[1] = pack_bf16x2(f23.x, f23.y);
-}
-
-// Eight 4-bit codes of a word (even element in the low nibble) minus a zero point, as
-// exact bf16x2 pairs d[j] = (k j, k j + 4).  zc = bf16x2 of 128 + min(z, 127); zc2 = bf16x2
-// of max(z - 127, 0), used only when `big`; magic = 0x43004300 (bf16x2 128, 128) held in a
-// register.
-template <bool kBig>
-__device__ __forceinline__ void nib8_minus_zero(uint32_t w, uint32_t zc, uint32_t zc2,
-                                                uint32_t magic, uint32_t (&d)[4]) {
-  // plain shifts (measured faster on sm_103a than high halves of products, which move
-  // them to the FMA pipe)
-  d[0] = sub_bf16x2(and_0f_or(w, magic), zc);
-  d[1] = sub_bf16x2(and_0f_or(w >> 4, magic), zc);
-  d[2] = sub_bf16x2(and_0f_or(w >> 8, magic), zc);
-  d[3] = sub_bf16x2(and_0f_or(w >> 12, magic), zc);
-  if constexpr (kBig) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) d[j] = sub_bf16x2(d[j], zc2);
-  }
-}
-
-}  // namespace
 
 namespace {
 
@@ -1210,10 +1177,6 @@ bool fact_ok(Fmt f, const GemvParams& p) {
 // ------------------------------------------------------------------ host side
 namespace {
 
-constexpr const char* fmt_name(Fmt f) {
-  return f == Fmt::I4G ? "I4G" : (f == Fmt::I4R ? "I4R" : (f == Fmt::I8R ? "I8R" : "MXFP4"));
-}
-
 template <Fmt F, int MT, bool FMA>
 cudaError_t launch_t(const GemvParams& p, int grid, cudaStream_t stream) {
   const size_t smem = (F == Fmt::MXFP4) ? sizeof(Routing) : 0;
@@ -1391,7 +1354,7 @@ cudaError_t launch_fact(const GemvParams& p, int num_sms, cudaStream_t stream) {
 template <Fmt F>
 cudaError_t launch_f(const GemvParams& p, int64_t rows, int grid, int num_sms, cudaStream_t stream) {
   if constexpr (F != Fmt::MXFP4) {
-    if (fact_ok(F, p))
+    if (fact_ok(F, p) && tuning(kKnobDecode) != 2)
       return rows <= 8 ? launch_fact<F, 1>(p, num_sms, stream) : launch_fact<F, 2>(p, num_sms, stream);
   }
   GemvParams q = p;

@@ -11,6 +11,9 @@ namespace wq {
 
 // Storage formats of the decode GEMV.
 enum class Fmt { I4G, I4R, I8R, MXFP4 };
+constexpr const char* fmt_name(Fmt f) {
+  return f == Fmt::I4G ? "I4G" : (f == Fmt::I4R ? "I4R" : (f == Fmt::I8R ? "I8R" : "MXFP4"));
+}
 
 struct GemvParams {
   const __nv_bfloat16* x;  // activations [M, K] (MXFP4: [R, K])
@@ -65,6 +68,16 @@ cudaError_t launch_gemv(Fmt f, GemvParams p, const GemvPlan& plan, cudaStream_t 
 // start reading them before the previous kernel of the stream has completed.
 void set_static_weights(int on);
 int static_weights();
+
+// The prepared group-wise 4-bit layout (gemv_prep.cu): the load-time repack and its
+// decode kernel (M <= 16, K % 256 == 0, groups of 128 codes or more).
+bool prep_shape_ok(int64_t M, int64_t N, int64_t K, int32_t group);
+size_t prep_bytes(int64_t N, int64_t K);
+size_t prep_ws_bytes(int64_t M, int64_t N, int64_t K, int num_sms);
+cudaError_t launch_prepare(const uint8_t* packed, const float* scale, const uint8_t* zero, int64_t N,
+                           int64_t K, int32_t group, uint8_t* out, cudaStream_t s);
+cudaError_t launch_prep(const GemvParams& p, const uint8_t* prep, void* workspace, size_t ws_bytes,
+                        int num_sms, cudaStream_t stream);
 
 // MXFP4 routing tables live in shared memory: bounded slot and expert counts.
 bool gemv_mxfp4_supported(int64_t R, int64_t S, int64_t E);
@@ -122,7 +135,7 @@ cudaError_t launch_gemm_tc(const GemmTcParams& p, int num_sms, cudaStream_t stre
 // Tuning knobs (wq_set_tuning): set by an explicit call, read with one relaxed atomic
 // load where a launch is planned; 0 means the library's own choice.
 enum Knob { kKnobGemvBlocks = 0, kKnobGemvClusters, kKnobGemvPush, kKnobGemvXsmem, kKnobGemmMinM,
-            kKnobCount };
+            kKnobDecode, kKnobPrep, kKnobPrepBlocksPerSM, kKnobCount };
 int64_t tuning(int knob);
 bool set_tuning(int knob, int64_t value);
 
