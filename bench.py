@@ -867,7 +867,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
-    ap.add_argument("--profile-case", choices=["decode_gate", "decode_down", "prefill_gate", "prefill_down", "mxfp4_gateup"],
+    ap.add_argument("--profile-case", choices=["decode_gate", "decode_down", "decode_k", "prefill_gate", "prefill_down",
+                                               "prefill_k", "mxfp4_gateup"],
                     help="run three launches of one kernel (for profiler captures) and exit")
     args = ap.parse_args()
     if args.impl == "reference":

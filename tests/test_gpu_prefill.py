@@ -1,7 +1,7 @@
 """The tensor-core regime at the benchmark's prefill sizes, against the CPU oracle.
 
 Llama-3.1-8B projection shapes at M = 2048 (gate 14336 x 4096; down 4096 x 14336, i.e.
-K = 14336 and 224 k steps; k and v 1024 x 4096 with split-K through the workspace) and
+K = 14336 and 224 k steps; k and v 1024 x 4096 on the 128 x 128 tiles) and
 M = 512 (gate), group 128, in the launch configuration the benchmark times (workspace
 sized by wq_linear_int4_groups_workspace).  The oracle computes sampled rows of x times
 sampled output columns that include the first and the last 256-wide column tiles and
@@ -52,14 +52,15 @@ def test_prefill_full_size_sampled(cuda_device, name, M):
     x = synth.normal_bf16((M, K), seed=M + K)
     bias = synth.normal_bf16((N,), seed=N + 3)
     nbytes = wq.wq_linear_int4_groups_workspace(M, N, K, G)
-    if name in ("k", "v"):
-        assert nbytes > 0, "k / v at M = 2048 have fewer tiles than SMs: split-K expected"
     ws = wq.alloc_workspace(nbytes, d)
     buf, y = guarded((M, N), torch.bfloat16, d)
     st = torch.zeros(1, dtype=torch.int32, device=d)
     wq.wq_linear_int4_groups(x.to(d), torch.from_numpy(packed).to(d), torch.from_numpy(scale).to(d),
                              torch.from_numpy(zero).to(d), bias.to(d), G, y=y, workspace=ws, dev_status=st)
     torch.cuda.synchronize()
+    if name in ("k", "v"):
+        # fewer 256 x 256 tiles than SMs: the 128 x 128 tiles, whole K, no partials
+        assert "tile=128" in wq.wq_last_launch() and nbytes == 0, wq.wq_last_launch()
     assert guards_intact(buf), "write outside y"
     assert int(st.item()) == 0
     if ws is not None:

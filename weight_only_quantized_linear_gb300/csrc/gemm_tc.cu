@@ -36,17 +36,23 @@ namespace wq {
 
 namespace {
 
-constexpr int kBM = 256;  // activation rows a tile (two 128-row accumulators)
-constexpr int kBN = 256;  // weight rows a tile
 constexpr int kBK = 64;   // k a stage: one 128-byte swizzle row of bf16
-constexpr int kStagesTc = 3;
-constexpr int kABytes = kBM * kBK * 2;    // 32 KB
-constexpr int kBBytes = kBN * kBK * 2;    // 32 KB
-constexpr int kPBytes = kBN * kBK / 2;    // 8 KB packed codes
-constexpr int kStageTcBytes = kABytes + kBBytes + kPBytes;
 constexpr int kDequantWarps = 8;
 constexpr int kThreadsTc = (2 + kDequantWarps) * 32;
-constexpr uint32_t kTmemCols = 512;
+constexpr size_t kSmemTcMax = 227 * 1024;
+
+// Tile geometry: kTile x kTile outputs (activation rows x weight rows), kTile / 128
+// accumulators of 128 rows in TMEM; stages as many as fit in shared memory (at most 6).
+template <int kTile>
+struct TileCfg {
+  static constexpr int kAcc = kTile / 128;
+  static constexpr int kABytes = kTile * kBK * 2;  // activation tile (bf16)
+  static constexpr int kBBytes = kTile * kBK * 2;  // dequantized weight tile (bf16)
+  static constexpr int kPBytes = kTile * kBK / 2;  // packed codes
+  static constexpr int kStageBytes = kABytes + kBBytes + kPBytes;
+  static constexpr int kStages = kTile == 256 ? 3 : 6;
+  static constexpr uint32_t kTmemCols = (uint32_t)(kAcc * kTile);
+};
 
 // ---- tcgen05 ----
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
@@ -123,20 +129,30 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 
 struct SharedTc {
-  uint64_t full_tma[kStagesTc];  // x + packed landed
-  uint64_t full_b[kStagesTc];    // dequantized weights written
-  uint64_t empty[kStagesTc];     // MMAs of the stage done
-  uint64_t acc_full;             // all MMAs done
+  uint64_t full_tma[6];  // x + packed landed
+  uint64_t full_b[6];    // dequantized weights written
+  uint64_t empty[6];     // MMAs of the stage done
+  uint64_t acc_full;     // all MMAs done
   uint32_t tmem_base;
   int abort;
 };
 
 }  // namespace
 
-template <bool kSplit>
+// kTile = 256: two 128 x 256 accumulators, each dequantized weight feeding 256 activation
+// rows (the large layers).  kTile = 128: one 128 x 128 accumulator and four times the
+// tiles, for layers with fewer 256 x 256 tiles than SMs (k and v at M = 2048), which
+// would otherwise split K and send f32 partials through HBM; the 256 dequantizing
+// threads then take half a weight row each.
+template <bool kSplit, int kTile>
 __global__ void __launch_bounds__(kThreadsTc, 1)
     k_gemm_w4g_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap pmap,
                   const GemmTcParams p) {
+  using C = TileCfg<kTile>;
+  constexpr int kStagesTc = C::kStages;
+  constexpr int kABytes = C::kABytes, kBBytes = C::kBBytes, kPBytes = C::kPBytes;
+  constexpr int kStageTcBytes = C::kStageBytes;
+  constexpr int kBM = kTile, kBN = kTile;
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
                                              ~uintptr_t(1023));
@@ -165,7 +181,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     fence_mbar_init();
     sh->abort = 0;
   }
-  if (warp == 1) tmem_alloc(&sh->tmem_base, kTmemCols);
+  if (warp == 1) tmem_alloc(&sh->tmem_base, C::kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -214,7 +230,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const uint32_t a_base = smem_u32(stage_a(s));
         const uint32_t b_base = smem_u32(stage_b(s));
 #pragma unroll
-        for (int acc = 0; acc < 2; ++acc) {
+        for (int acc = 0; acc < C::kAcc; ++acc) {
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             // +32 bytes a 16-element k slice inside the 128-byte swizzled rows
@@ -229,7 +245,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     }
   } else {
     // ================= dequantize (8 warps), then epilogue =================
-    const int t = threadIdx.x - 64;  // weight row of the tile owned by this thread
+    // kTile 256: thread t owns weight row t, all 64 codes of a stage; kTile 128: row
+    // t % 128, codes 32 (t / 128) .. + 31
+    const int tt = threadIdx.x - 64;
+    const int t = (kTile == 256) ? tt : (tt & 127);
+    const int half = (kTile == 256) ? 0 : (tt >> 7);
     const int64_t n = imin64(n0 + t, N - 1);
     const int gshift = __ffs(p.group) - 1;
     const uint32_t gpr = (uint32_t)(K >> gshift);  // groups a row (K < 2^31)
@@ -276,7 +296,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 
     const uint32_t prow = (uint32_t)t * 32;  // packed row, 32-byte swizzle
     const uint32_t pswz = (uint32_t)((t >> 2) & 1);
-    // this thread's eight 16-byte pieces of its dequantized row: piece w at w ^ (row mod 8)
+    // this thread's 16-byte pieces of its dequantized row: piece w at w ^ (row mod 8)
     // (128-byte swizzle), offsets inside a stage
     uint32_t boff[8];
 #pragma unroll
@@ -286,17 +306,32 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     // one k step: the packed row from the stage, dequantized, into the MMA's layout
     auto dequant_step = [&](int s, const Nib8Consts& k0, const Nib8Consts& k1) {
       const uint32_t pbase = smem_u32(stage_p(s));
-      const uint4 c0 = ld_shared_v4(pbase + pa0);
-      const uint4 c1 = ld_shared_v4(pbase + pa1);
-      const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
       const uint32_t bbase = smem_u32(stage_b(s));
+      if constexpr (kTile == 256) {
+        const uint4 c0 = ld_shared_v4(pbase + pa0);
+        const uint4 c1 = ld_shared_v4(pbase + pa1);
+        const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
-      for (int w = 0; w < 8; ++w) {
-        uint32_t o[4];
-        dequant_nib8(words[w], (w < 4) ? k0 : k1, o);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(bbase + boff[w]), "r"(o[0]),
-                     "r"(o[1]), "r"(o[2]), "r"(o[3])
-                     : "memory");
+        for (int w = 0; w < 8; ++w) {
+          uint32_t o[4];
+          dequant_nib8(words[w], (w < 4) ? k0 : k1, o);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(bbase + boff[w]), "r"(o[0]),
+                       "r"(o[1]), "r"(o[2]), "r"(o[3])
+                       : "memory");
+        }
+      } else {
+        // codes 32 half .. 32 half + 31: the packed 16-byte unit `half` of the row
+        const uint4 c = ld_shared_v4(pbase + (half ? pa1 : pa0));
+        const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+        const Nib8Consts& kc = half ? k1 : k0;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          uint32_t o[4];
+          dequant_nib8(words[w], kc, o);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(bbase + boff[4 * half + w]),
+                       "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
+                       : "memory");
+        }
       }
     };
 
@@ -333,16 +368,20 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       atomicExch(&sh->abort, 1);
     }
     tc_fence_after();
-    const int q = warp & 3;          // TMEM lane quarter this warp may read
-    const int acc = (warp - 2) >> 2; // accumulator (activation rows 0..127 or 128..255)
+    const int q = warp & 3;  // TMEM lane quarter this warp may read
+    // kTile 256: accumulator (warp - 2) / 4, all 256 columns; kTile 128: the one
+    // accumulator, columns 64 ((warp - 2) / 4) .. + 63
+    const int acc = (kTile == 256) ? ((warp - 2) >> 2) : 0;
+    const int col0 = (kTile == 256) ? 0 : ((warp - 2) >> 2) * 64;
+    constexpr int kChunks = (kTile == 256) ? kBN / 32 : 2;
     const int64_t m = m0 + acc * 128 + q * 32 + lane;
     const bool vec_ok = (N % 8 == 0) && ((reinterpret_cast<uintptr_t>(p.y) & 15) == 0);
     constexpr bool split = kSplit;  // f32 partials to the workspace, no bias
 #pragma unroll 1
-    for (int ch = 0; ch < kBN / 32; ++ch) {
+    for (int ch = 0; ch < kChunks; ++ch) {
       uint32_t r[32];
-      tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + acc * kBN + ch * 32, r);
-      const int64_t nb = n0 + ch * 32;
+      tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + acc * kBN + col0 + ch * 32, r);
+      const int64_t nb = n0 + col0 + ch * 32;
       if (split && m < M && nb < N) {
         // f32 partial sums of this k range, no bias (the reduction adds it)
         float* dst = p.part + ((int64_t)blockIdx.z * M + m) * N + nb;
@@ -388,7 +427,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
@@ -457,8 +496,18 @@ __global__ void __launch_bounds__(256) k_splitk_reduce(float* __restrict__ part,
 }
 
 // ------------------------------------------------------------------ host side
+namespace {
+// 256 x 256 tiles when they fill at least half the SMs; else 128 x 128 tiles (four times
+// as many, no f32 partials through HBM), split along K only if even those are too few.
+int gemm_tile(int64_t M, int64_t N, int num_sms) {
+  const int64_t t256 = ((M + 255) / 256) * ((N + 255) / 256);
+  return t256 * 2 > num_sms ? 256 : 128;
+}
+}  // namespace
+
 int gemm_tc_splits(int64_t M, int64_t N, int64_t K, int num_sms) {
-  const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
+  const int tile = gemm_tile(M, N, num_sms);
+  const int64_t tiles = ((M + tile - 1) / tile) * ((N + tile - 1) / tile);
   const int64_t nk = (K + kBK - 1) / kBK;
   if (tiles * 2 > num_sms) return 1;
   // as many k ranges as fill the SMs, each of at least 8 k steps, at most 8 ranges
@@ -481,42 +530,46 @@ bool gemm_tc_supported(int64_t M, int64_t N, int64_t K, int32_t group) {
          K % group == 0 && M <= (int64_t(1) << 31) && N <= (int64_t(1) << 31);
 }
 
-cudaError_t launch_gemm_tc(const GemmTcParams& p, int num_sms, cudaStream_t stream) {
+namespace {
+template <int kTile>
+cudaError_t launch_gemm_tile(const GemmTcParams& p, int splits, cudaStream_t stream) {
+  using C = TileCfg<kTile>;
   CUtensorMap xmap, pmap;
   if (!encode_tensor_map_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                             const_cast<__nv_bfloat16*>(p.x), (uint64_t)p.K, (uint64_t)p.M,
-                            (uint64_t)p.K * 2, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B))
+                            (uint64_t)p.K * 2, kBK, kTile, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   if (!encode_tensor_map_2d(&pmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t*>(p.packed),
-                            (uint64_t)p.K / 2, (uint64_t)p.N, (uint64_t)p.K / 2, kBK / 2, kBN,
+                            (uint64_t)p.K / 2, (uint64_t)p.N, (uint64_t)p.K / 2, kBK / 2, kTile,
                             CU_TENSOR_MAP_SWIZZLE_32B))
     return cudaErrorInvalidValue;
-  const size_t smem = 1024 + (size_t)kStagesTc * kStageTcBytes + sizeof(SharedTc);
+  const size_t smem = 1024 + (size_t)C::kStages * C::kStageBytes + sizeof(SharedTc);
+  static_assert(1024 + (size_t)C::kStages * C::kStageBytes + sizeof(SharedTc) <= kSmemTcMax,
+                "GEMM stages exceed shared memory");
   static std::atomic<uint64_t> attr_set{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
   if (!(attr_set.load(std::memory_order_acquire) & bit)) {
-    e = cudaFuncSetAttribute(k_gemm_w4g_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(k_gemm_w4g_tc<false, kTile>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_gemm_w4g_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(k_gemm_w4g_tc<true, kTile>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
     if (e != cudaSuccess) return e;
     attr_set.fetch_or(bit, std::memory_order_release);
   }
-  const int splits = (p.part != nullptr) ? std::max(1, (int)p.splits) : 1;
   GemmTcParams q = p;
   if (splits == 1) q.part = nullptr;
-  const dim3 grid((unsigned)((p.M + kBM - 1) / kBM), (unsigned)((p.N + kBN - 1) / kBN),
+  const dim3 grid((unsigned)((p.M + kTile - 1) / kTile), (unsigned)((p.N + kTile - 1) / kTile),
                   (unsigned)splits);
-  note_launch("k_gemm_w4g_tc<%s> grid=%ux%ux%u%s", splits > 1 ? "split" : "unsplit", grid.x, grid.y,
-              grid.z, splits > 1 ? " + k_splitk_reduce" : "");
+  note_launch("k_gemm_w4g_tc<%s,tile=%d> grid=%ux%ux%u%s", splits > 1 ? "split" : "unsplit", kTile, grid.x,
+              grid.y, grid.z, splits > 1 ? " + k_splitk_reduce" : "");
   if (splits == 1)
-    k_gemm_w4g_tc<false><<<grid, kThreadsTc, smem, stream>>>(xmap, pmap, q);
+    k_gemm_w4g_tc<false, kTile><<<grid, kThreadsTc, smem, stream>>>(xmap, pmap, q);
   else
-    k_gemm_w4g_tc<true><<<grid, kThreadsTc, smem, stream>>>(xmap, pmap, q);
+    k_gemm_w4g_tc<true, kTile><<<grid, kThreadsTc, smem, stream>>>(xmap, pmap, q);
   e = cudaGetLastError();
   if (e != cudaSuccess || splits == 1) return e;
   // splits > 1 only with at most num_sms / 2 tiles, so M <= 256 * num_sms / 2 rows: within
@@ -524,6 +577,13 @@ cudaError_t launch_gemm_tc(const GemmTcParams& p, int num_sms, cudaStream_t stre
   const dim3 rgrid((unsigned)((p.N + 1023) / 1024), (unsigned)p.M);
   k_splitk_reduce<<<rgrid, 256, 0, stream>>>(q.part, splits, p.M, p.N, p.bias, p.y);
   return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_gemm_tc(const GemmTcParams& p, int num_sms, cudaStream_t stream) {
+  const int splits = (p.part != nullptr) ? std::max(1, (int)p.splits) : 1;
+  return gemm_tile(p.M, p.N, num_sms) == 256 ? launch_gemm_tile<256>(p, splits, stream)
+                                             : launch_gemm_tile<128>(p, splits, stream);
 }
 
 }  // namespace wq
