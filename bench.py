@@ -352,7 +352,32 @@ def run_variants(dev, peaks, stream):
             nbytes = touched * N * K * (0.5 + 1 / 32) + 2 * R * K + 2 * R * S * N
             gbs = nbytes / (us * 1e-6) / 1e9
             mx[f"N={N} R={R}"] = {"us": round(us, 2), "experts_touched": round(touched, 2), "gbs": round(gbs, 1),
-                                  "frac_of_hbm_peak": round(gbs / hbm, 4)}
+                                  "frac_of_hbm_peak": round(gbs / hbm, 4), "kernel": wq.wq_last_launch()}
+            # the combine form (softmax weights over the four slots, y [R, N]) and the per-slot
+            # form (x [R, S, K]): the same weight bytes
+            weights = [torch.softmax(synth.routing_topk(R, E, S, seed=900 + R + j)[1], -1).to(dev) for j in range(8)]
+            yc = torch.empty((R, N), dtype=torch.bfloat16, device=dev)
+            wsc = torch.empty(wq.wq_mxfp4_combine_experts_workspace(R, S, E, N, K), dtype=torch.uint8, device=dev)
+
+            def call_c(i, copies=copies, routes=routes, weights=weights, x=x, yc=yc, wsc=wsc):
+                b_, s_ = copies[i % 2]
+                wq.wq_mxfp4_combine_experts(x, b_, s_, routes[i % 8], weights[i % 8], y=yc, workspace=wsc,
+                                            stream=stream)
+
+            us_c = time_rotating(call_c, 32, stream)
+            gbs_c = (nbytes - 2 * R * S * N + 2 * R * N) / (us_c * 1e-6) / 1e9
+            mx[f"combine N={N} R={R}"] = {"us": round(us_c, 2), "gbs": round(gbs_c, 1),
+                                          "frac_of_hbm_peak": round(gbs_c / hbm, 4)}
+            xs_ = synth.normal_bf16((R, S, K), seed=12, device="cpu").to(dev)
+
+            def call_s(i, copies=copies, routes=routes, xs_=xs_, y=y):
+                b_, s_ = copies[i % 2]
+                wq.wq_mxfp4_experts(xs_, b_, s_, routes[i % 8], y=y, stream=stream)
+
+            us_s = time_rotating(call_s, 32, stream)
+            gbs_s = (nbytes + 2 * R * (S - 1) * K) / (us_s * 1e-6) / 1e9
+            mx[f"per-slot N={N} R={R}"] = {"us": round(us_s, 2), "gbs": round(gbs_s, 1),
+                                           "frac_of_hbm_peak": round(gbs_s / hbm, 4)}
     torch.cuda.synchronize()
     if int(st.item()) != 0:
         raise RuntimeError(f"quantize/pack device status {int(st.item())}")
@@ -813,8 +838,9 @@ def run_gpu(args):
 
 def run_profile_case(args):
     """A few launches of one kernel on one projection, for profiler captures: decode_gate /
-    decode_down (M = 1, workspace on, as timed above), prefill_gate / prefill_down (M = 2048) or
-    mxfp4_gateup (MXFP4 experts, one row routed to 4 of 32)."""
+    decode_down / decode_k (M = 1, workspace on, as timed above), prepared_down (M = 1 on the
+    repacked layout), prefill_gate / prefill_down / prefill_k (M = 2048) or mxfp4_gateup (MXFP4
+    experts, one row routed to 4 of 32)."""
     import torch
 
     import weight_only_quantized_linear_gb300 as wq
@@ -839,7 +865,7 @@ def run_profile_case(args):
         return 0
     kind, proj = args.profile_case.split("_")
     N, K = synth.LLAMA_PROJ[proj]
-    M = 1 if kind == "decode" else PREFILL_M
+    M = PREFILL_M if kind == "prefill" else 1
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     w = synth.weight_f32(N, K, seed=1000, outlier_frac=0.001, device=dev)
     codes, scale, zero = wq.wq_quantize_groups(w, GROUP, 4, wq.WQ_ASYM, dev_status=st)
@@ -847,9 +873,16 @@ def run_profile_case(args):
     del w, codes
     x = synth.normal_bf16((M, K), seed=5, device="cpu").to(dev)
     y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-    ws = wq.alloc_workspace(wq.wq_linear_int4_groups_workspace(M, N, K, GROUP), dev)
-    for _ in range(3):
-        wq.wq_linear_int4_groups(x, packed, scale, zero, None, GROUP, y=y, workspace=ws, dev_status=st)
+    if kind == "prepared":
+        # the decode step on the load-time repacked layout (the repack itself is not timed)
+        prep = wq.wq_prepare_int4_groups(packed, scale, zero, GROUP)
+        ws = wq.alloc_workspace(wq.wq_linear_int4_groups_prepared_workspace(M, N, K, GROUP), dev)
+        for _ in range(3):
+            wq.wq_linear_int4_groups_prepared(x, prep, N, None, GROUP, y=y, workspace=ws, dev_status=st)
+    else:
+        ws = wq.alloc_workspace(wq.wq_linear_int4_groups_workspace(M, N, K, GROUP), dev)
+        for _ in range(3):
+            wq.wq_linear_int4_groups(x, packed, scale, zero, None, GROUP, y=y, workspace=ws, dev_status=st)
     torch.cuda.synchronize()
     if int(st.item()) != 0:
         raise RuntimeError(f"device status {int(st.item())}")
@@ -868,7 +901,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--profile-case", choices=["decode_gate", "decode_down", "decode_k", "prefill_gate", "prefill_down",
-                                               "prefill_k", "mxfp4_gateup"],
+                                               "prefill_k", "prepared_down", "mxfp4_gateup"],
                     help="run three launches of one kernel (for profiler captures) and exit")
     args = ap.parse_args()
     if args.impl == "reference":
