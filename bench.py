@@ -851,9 +851,9 @@ def run_profile_case(args):
     wq.build()
     if args.profile_case == "mxfp4_gateup":
         # MXFP4 experts, shared input: E = 32, gate/up N = 5760, K = 2880, one row, top-4
-        E, N, K, S, R = 32, 5760, 2880, 4, 1
+        E, N, K, S, R = 32, 5760, 2880, 4, args.profile_rows
         blocks, scales = synth.mxfp4_experts(E, N, K, seed=800, device=dev)
-        route = synth.routing_topk(R, E, S, seed=901, device=dev)[0]
+        route = synth.routing_topk(R, E, S, seed=900 + R + 1, device=dev)[0]
         x = synth.normal_bf16((R, 1, K), seed=11, device="cpu").to(dev)
         y = torch.empty((R, S, N), dtype=torch.bfloat16, device=dev)
         wsb = wq.wq_mxfp4_experts_shared_workspace(R, S, E, N, K)
@@ -900,6 +900,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--profile-rows", type=int, default=1, help="routed rows R of the mxfp4_gateup profile case")
     ap.add_argument("--profile-case", choices=["decode_gate", "decode_down", "decode_k", "prefill_gate", "prefill_down",
                                                "prefill_k", "prepared_down", "mxfp4_gateup"],
                     help="run three launches of one kernel (for profiler captures) and exit")

@@ -1298,7 +1298,7 @@ cudaError_t launch_fact(const GemvParams& p, int num_sms, cudaStream_t stream) {
     const int64_t q = items / clusters;
     for (int64_t icnt = std::max<int64_t>(q, 1); icnt <= q + 1; ++icnt) {
       const uint64_t U = (uint64_t)(icnt * spt);
-      auto bound = [&](uint64_t w) { return (w * U) >> 6; };
+      auto bound = [&](uint64_t w) { return (w * U) >> kFactWarpsLog2; };
       auto owner = [&](uint64_t u) {
         uint64_t w = 0;
         while (w + 1 < (uint64_t)kFactWarps && bound(w + 1) <= u) ++w;
