@@ -1356,6 +1356,12 @@ cudaError_t launch_f(const GemvParams& p, int64_t rows, int grid, int num_sms, c
   if constexpr (F != Fmt::MXFP4) {
     if (fact_ok(F, p) && tuning(kKnobDecode) != 2)
       return rows <= 8 ? launch_fact<F, 1>(p, num_sms, stream) : launch_fact<F, 2>(p, num_sms, stream);
+  } else {
+    // MXFP4: the TMA-ring cluster kernel (gemv_mx.cu) where its shape rules hold
+    if (gemv_mx_ok(p) && tuning(kKnobDecode) != 2) {
+      const cudaError_t e = launch_gemv_mx(p, num_sms, stream);
+      if (e != cudaErrorNotSupported) return e;
+    }
   }
   GemvParams q = p;
   if (q.order != nullptr) {  // the exact kernel reads activations from global memory

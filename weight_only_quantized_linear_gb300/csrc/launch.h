@@ -81,6 +81,11 @@ cudaError_t launch_prep(const GemvParams& p, const uint8_t* prep, void* workspac
 
 // MXFP4 routing tables live in shared memory: bounded slot and expert counts.
 bool gemv_mxfp4_supported(int64_t R, int64_t S, int64_t E);
+// The MXFP4 TMA-ring cluster kernel (gemv_mx.cu): N a multiple of 16, 768 <= K <= 8192,
+// at most 1024 slots and 256 experts, 16-byte aligned codes, scales and activations.
+// launch_gemv_mx returns cudaErrorNotSupported when its shared memory does not fit.
+bool gemv_mx_ok(const GemvParams& p);
+cudaError_t launch_gemv_mx(const GemvParams& p, int num_sms, cudaStream_t stream);
 
 // Load-time and test kernels (quant.cu).
 cudaError_t launch_quantize(const float* w, int64_t N, int64_t K, int32_t G, int32_t bits,
