@@ -554,10 +554,14 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM) k_gemv(const GemvParam
 
 namespace {
 
-// The factored kernel runs in clusters of kFactCluster CTAs (kFactWarps warps).
-constexpr int kFactCluster = 8;
+// The factored kernel runs in clusters of kFactCluster CTAs (kFactWarps warps).  Two:
+// the main loop is bound by instruction issue, so the launch should put the same two CTAs
+// on every SM, which clusters of two do; clusters of eight fit only 34 to a launch on
+// GB300 (272 CTAs on 152 SMs, a fifth of the SMs with one CTA whose warps finish early).
+// Measured on the Llama-3.1-8B decode layer: 61.6 us against 64.1 us with clusters of 8.
+constexpr int kFactCluster = 2;
 constexpr int kFactWarps = kFactCluster * kWarps;
-constexpr int kFactWarpsLog2 = 6;
+constexpr int kFactWarpsLog2 = 4;
 static_assert((1 << kFactWarpsLog2) == kFactWarps, "warps a cluster: a power of two");
 
 // Write a finished tile's D fragments (rows g8 / g8 + 8, columns 2cq, 2cq + 1 of each
@@ -1276,23 +1280,19 @@ cudaError_t launch_fact(const GemvParams& p, int num_sms, cudaStream_t stream) {
       return cudaErrorInvalidValue;
     maps.z = maps.s;  // unused
   }
-  // clusters: at most nine tenths of those co-resident (a fixed 2 blocks an SM on 152 SMs
-  // bounds it; the launch clamps to the measured figure), at least kFactMinSteps steps a
-  // warp on average (fewer, fuller warps beat many idle ones), never more than there are
-  // items
+  // clusters: every co-resident one (two blocks an SM; the launch clamps to the figure the
+  // occupancy query gives), but at least kFactMinSteps steps a warp on average (fewer,
+  // fuller warps beat many idle ones), never more than there are items
   constexpr int64_t kBatch = 8 * MT;
   const int64_t items = ((p.N + kRows - 1) / kRows) * ((p.M + kBatch - 1) / kBatch);
   const int64_t spt = row_bytes / (2 * kChunkBytes);
-  // Nine tenths of the clusters two blocks an SM would hold: measured on GB300, 34 clusters
-  // of 8 beat 36 to 38 by 4 to 10 % on the 14336 x 4096 and 4096 x 14336 layers (with 36
-  // or more, the last clusters of a launch start late).
-  int64_t cap = std::min<int64_t>((int64_t)num_sms * kBlocksPerSM * 9 / (10 * kFactCluster),
+  int64_t cap = std::min<int64_t>((int64_t)num_sms * kBlocksPerSM / kFactCluster,
                                   std::max<int64_t>(1, items * spt / (kFactWarps * kFactMinSteps)));
   if (const int64_t v = tuning(kKnobGemvClusters); v >= 1) cap = v;  // tuning and test knob
   const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(cap, items));
   // push fixup: receive slots a warp = the most warps any cut tile meets, from the same
   // split as the kernel (cluster c takes q or q + 1 items; warp w of a cluster starts at
-  // unit (w * U) >> 6)
+  // unit (w * U) >> kFactWarpsLog2)
   uint32_t cmax = 1;
   {
     const int64_t q = items / clusters;
