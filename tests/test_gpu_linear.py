@@ -409,12 +409,14 @@ def test_decode_offset_activations_full_range_zero_points(cuda_device, M, fmt):
 @pytest.mark.parametrize("mode", ["push", "barrier", "default"])
 @pytest.mark.parametrize("M,N,K,clusters", [(1, 14336, 4096, None), (1, 4096, 14336, None), (1, 1024, 4096, None),
                                             (1, 4096, 4096, None), (4, 1000, 6144, 5), (12, 700, 4096, None),
-                                            (1, 256, 2048, 3)])
+                                            (1, 256, 2048, 3), (1, 1000, 8192, 7), (2, 600, 16384, None),
+                                            (3, 4100, 8192, 200)])
 def test_factored_cut_tile_fixup(cuda_device, tune, mode, M, N, K, clusters):
     """Tiles cut between warps are finished either by pushes into the closing warp's
     shared memory (no cluster-wide barrier) or by the closing warp reading the parked
-    partials after cluster barriers (forced each way, and the launch's own choice); all
-    match the oracle and are deterministic."""
+    partials after cluster barriers (forced each way, and the launch's own choice), with
+    clusters of two CTAs and, for rows of 32 or more steps (K >= 8192), of four; all match
+    the oracle and are deterministic."""
     if mode == "push":
         tune(wq.WQ_TUNE_GEMV_PUSH, 1)
     elif mode == "barrier":

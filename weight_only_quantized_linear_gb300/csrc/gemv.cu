@@ -554,15 +554,20 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM) k_gemv(const GemvParam
 
 namespace {
 
-// The factored kernel runs in clusters of kFactCluster CTAs (kFactWarps warps).  Two:
-// the main loop is bound by instruction issue, so the launch should put the same two CTAs
-// on every SM, which clusters of two do; clusters of eight fit only 34 to a launch on
-// GB300 (272 CTAs on 152 SMs, a fifth of the SMs with one CTA whose warps finish early).
-// Measured on the Llama-3.1-8B decode layer: 61.6 us against 64.1 us with clusters of 8.
-constexpr int kFactCluster = 2;
-constexpr int kFactWarps = kFactCluster * kWarps;
-constexpr int kFactWarpsLog2 = 4;
-static_assert((1 << kFactWarpsLog2) == kFactWarps, "warps a cluster: a power of two");
+// The factored kernel runs in clusters of kCl CTAs (kCl * kWarps warps), as many as
+// fit two blocks on every SM: the main loop is bound by instruction issue, so every SM
+// should hold the same two CTAs.  Two CTAs a cluster, four for group-wise rows of 32 or
+// more steps (K >= 8192 at one batch); clusters of eight fit only 34 to a launch on GB300
+// (272 CTAs on 152 SMs, a fifth of the SMs with one CTA whose warps finish early).
+// Measured on the Llama-3.1-8B decode layer (clusters of 8 / 4 / 2): 64.1 / 62.4 / 61.6 us
+// a layer; down (4096 x 14336) 13.87 / 13.4 / 13.85 us.
+template <int kCl>
+struct ClusterShape {
+  static constexpr int kWarpsC = kCl * kWarps;
+  static constexpr int kLog2 = kCl == 2 ? 4 : (kCl == 4 ? 5 : 6);
+  static_assert((1 << kLog2) == kWarpsC, "warps a cluster: a power of two");
+};
+__host__ __device__ constexpr int cluster_warps_log2(int cl) { return cl == 2 ? 4 : (cl == 4 ? 5 : 6); }
 
 // Write a finished tile's D fragments (rows g8 / g8 + 8, columns 2cq, 2cq + 1 of each
 // group of 8 activation rows) to y, adding the bias.
@@ -634,9 +639,11 @@ __host__ __device__ constexpr int fact_ring_bytes(int kSD) {
 // order of the MMA fragments ([row][k / 128][(k / 8) % 4][(k / 32) % 4] 16-byte pieces
 // holding (x0, x4) (x1, x5) (x2, x6) (x3, x7)), so that a lane's B fragments are four
 // 16-byte shared loads a chunk, with no shuffles and no global-memory latency in the loop.
-template <Fmt F, int MT, int kSD, bool kXS, bool kPush>
+template <Fmt F, int MT, int kSD, bool kXS, bool kPush, int kCl>
 __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     k_gemv_fact(const GemvParams p, const __grid_constant__ FactMaps maps, const FactGeom geo) {
+  constexpr int kFactWarps = ClusterShape<kCl>::kWarpsC;
+  constexpr int kFactWarpsLog2 = ClusterShape<kCl>::kLog2;
   const uint32_t xstride = geo.xstride;
   static_assert(F == Fmt::I4G || F == Fmt::I4R || F == Fmt::I8R, "affine formats only");
   constexpr int kPiece = piece_k<F>();   // k of a lane's 16 bytes
@@ -1202,9 +1209,10 @@ constexpr int kMaxDevicesGemv = 64;
 constexpr size_t kSmemPerSMFact = 228 * 1024;
 constexpr size_t kFactStaticBytes = (size_t)kWarps * 2 * 32 * 4 * sizeof(float);
 
-template <Fmt F, int MT, int kSD, bool kXS, bool kPush>
+template <Fmt F, int MT, int kSD, bool kXS, bool kPush, int kCl>
 cudaError_t launch_fact_t(const GemvParams& p, const FactMaps& maps, const FactGeom& geo,
                           size_t smem, int64_t clusters, int num_sms, cudaStream_t stream) {
+  constexpr int kFactCluster = kCl;
   // co-resident clusters a device for the last dynamic shared-memory size (0: unknown)
   static int active[kMaxDevicesGemv] = {0};
   static size_t active_smem[kMaxDevicesGemv] = {0};
@@ -1213,7 +1221,7 @@ cudaError_t launch_fact_t(const GemvParams& p, const FactMaps& maps, const FactG
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevicesGemv) dev = 0;
   const uint64_t bit = 1ull << dev;
   if (!(smem_set.load(std::memory_order_acquire) & bit)) {
-    const cudaError_t e = cudaFuncSetAttribute(k_gemv_fact<F, MT, kSD, kXS, kPush>,
+    const cudaError_t e = cudaFuncSetAttribute(k_gemv_fact<F, MT, kSD, kXS, kPush, kCl>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                (int)(kSmemPerSMFact / 2));
     if (e != cudaSuccess) return e;
@@ -1237,7 +1245,7 @@ cudaError_t launch_fact_t(const GemvParams& p, const FactMaps& maps, const FactG
   if (active[dev] == 0 || active_smem[dev] != smem) {
     cfg.gridDim = dim3(kFactCluster * (unsigned)num_sms);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, k_gemv_fact<F, MT, kSD, kXS, kPush>, &cfg) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveClusters(&n, k_gemv_fact<F, MT, kSD, kXS, kPush, kCl>, &cfg) != cudaSuccess ||
         n <= 0) {
       (void)cudaGetLastError();
       n = num_sms * kBlocksPerSM / kFactCluster;
@@ -1251,7 +1259,19 @@ cudaError_t launch_fact_t(const GemvParams& p, const FactMaps& maps, const FactG
   note_launch("k_gemv_fact<%s,MT=%d,stages=%d,%s,%s> grid=%u (%lld clusters of %d) smem=%zu",
               fmt_name(F), MT, kSD, kXS ? "x staged" : "x global", kPush ? "push fixup" : "barrier fixup",
               cfg.gridDim.x, (long long)std::max<int64_t>(1, clusters), kFactCluster, smem);
-  return cudaLaunchKernelEx(&cfg, k_gemv_fact<F, MT, kSD, kXS, kPush>, p, maps, geo);
+  return cudaLaunchKernelEx(&cfg, k_gemv_fact<F, MT, kSD, kXS, kPush, kCl>, p, maps, geo);
+}
+
+// Clusters of four for group-wise 4-bit at one batch with long rows, else two (the host
+// split above was computed for the same size).
+template <Fmt F, int MT, int kSD, bool kXS, bool kPush>
+cudaError_t launch_fact_c(int cl, const GemvParams& p, const FactMaps& maps, const FactGeom& geo,
+                          size_t smem, int64_t clusters, int num_sms, cudaStream_t stream) {
+  if constexpr (F == Fmt::I4G && MT == 1) {
+    if (cl == 4)
+      return launch_fact_t<F, MT, kSD, kXS, kPush, 4>(p, maps, geo, smem, clusters, num_sms, stream);
+  }
+  return launch_fact_t<F, MT, kSD, kXS, kPush, 2>(p, maps, geo, smem, clusters, num_sms, stream);
 }
 
 // Ring depth and activation staging: four stages a warp; activations staged in shared
@@ -1286,22 +1306,25 @@ cudaError_t launch_fact(const GemvParams& p, int num_sms, cudaStream_t stream) {
   constexpr int64_t kBatch = 8 * MT;
   const int64_t items = ((p.N + kRows - 1) / kRows) * ((p.M + kBatch - 1) / kBatch);
   const int64_t spt = row_bytes / (2 * kChunkBytes);
-  int64_t cap = std::min<int64_t>((int64_t)num_sms * kBlocksPerSM / kFactCluster,
-                                  std::max<int64_t>(1, items * spt / (kFactWarps * kFactMinSteps)));
+  const int cl = (F == Fmt::I4G && MT == 1 && spt >= 32) ? 4 : 2;  // CTAs a cluster
+  const int cl_log2 = cluster_warps_log2(cl);
+  const int64_t cl_warps = (int64_t)cl * kWarps;
+  int64_t cap = std::min<int64_t>((int64_t)num_sms * kBlocksPerSM / cl,
+                                  std::max<int64_t>(1, items * spt / (cl_warps * kFactMinSteps)));
   if (const int64_t v = tuning(kKnobGemvClusters); v >= 1) cap = v;  // tuning and test knob
   const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(cap, items));
   // push fixup: receive slots a warp = the most warps any cut tile meets, from the same
   // split as the kernel (cluster c takes q or q + 1 items; warp w of a cluster starts at
-  // unit (w * U) >> kFactWarpsLog2)
+  // unit (w * U) >> log2(warps a cluster))
   uint32_t cmax = 1;
   {
     const int64_t q = items / clusters;
     for (int64_t icnt = std::max<int64_t>(q, 1); icnt <= q + 1; ++icnt) {
       const uint64_t U = (uint64_t)(icnt * spt);
-      auto bound = [&](uint64_t w) { return (w * U) >> kFactWarpsLog2; };
+      auto bound = [&](uint64_t w) { return (w * U) >> cl_log2; };
       auto owner = [&](uint64_t u) {
         uint64_t w = 0;
-        while (w + 1 < (uint64_t)kFactWarps && bound(w + 1) <= u) ++w;
+        while (w + 1 < (uint64_t)cl_warps && bound(w + 1) <= u) ++w;
         return w;
       };
       for (int64_t t = 0; t < icnt; ++t) {
@@ -1325,13 +1348,13 @@ cudaError_t launch_fact(const GemvParams& p, int num_sms, cudaStream_t stream) {
     const size_t xbytes = ((size_t)p.M * xstride + 15) & ~size_t(15);
     const FactGeom geo{xstride, cmax};
     if (x_ok && push_ok && fits(ring4 + xbytes + recv))
-      return launch_fact_t<F, MT, 4, true, true>(p, maps, geo, ring4 + xbytes + recv, clusters, num_sms, stream);
+      return launch_fact_c<F, MT, 4, true, true>(cl, p, maps, geo, ring4 + xbytes + recv, clusters, num_sms, stream);
     if (x_ok && push_ok && fits(ring3 + xbytes + recv))
-      return launch_fact_t<F, MT, 3, true, true>(p, maps, geo, ring3 + xbytes + recv, clusters, num_sms, stream);
+      return launch_fact_c<F, MT, 3, true, true>(cl, p, maps, geo, ring3 + xbytes + recv, clusters, num_sms, stream);
     if (x_ok && fits(ring4 + xbytes))
-      return launch_fact_t<F, MT, 4, true, false>(p, maps, geo, ring4 + xbytes, clusters, num_sms, stream);
+      return launch_fact_c<F, MT, 4, true, false>(cl, p, maps, geo, ring4 + xbytes, clusters, num_sms, stream);
     if (x_ok && fits(ring3 + xbytes))
-      return launch_fact_t<F, MT, 3, true, false>(p, maps, geo, ring3 + xbytes, clusters, num_sms, stream);
+      return launch_fact_c<F, MT, 3, true, false>(cl, p, maps, geo, ring3 + xbytes, clusters, num_sms, stream);
   }
   const FactGeom geo{0, cmax};
   // activations read from global memory: an activation order is gathered first
@@ -1344,8 +1367,8 @@ cudaError_t launch_fact(const GemvParams& p, int num_sms, cudaStream_t stream) {
     q.order = nullptr;
   }
   if (push_ok && fits(ring4 + recv))
-    return launch_fact_t<F, MT, 4, false, true>(q, maps, geo, ring4 + recv, clusters, num_sms, stream);
-  return launch_fact_t<F, MT, 4, false, false>(q, maps, geo, ring4, clusters, num_sms, stream);
+    return launch_fact_c<F, MT, 4, false, true>(cl, q, maps, geo, ring4 + recv, clusters, num_sms, stream);
+  return launch_fact_c<F, MT, 4, false, false>(cl, q, maps, geo, ring4, clusters, num_sms, stream);
 }
 
 // I4G with a group of at least 128 codes, I4R, I8R: the factored kernel (warp MMA,
