@@ -378,6 +378,24 @@ def run_variants(dev, peaks, stream):
             gbs_s = (nbytes + 2 * R * (S - 1) * K) / (us_s * 1e-6) / 1e9
             mx[f"per-slot N={N} R={R}"] = {"us": round(us_s, 2), "gbs": round(gbs_s, 1),
                                            "frac_of_hbm_peak": round(gbs_s / hbm, 4)}
+        # many routed rows (prefill / serving batches): the grouped tensor-core GEMM, its
+        # four launches (routing tables, gather, GEMM) timed together; dense-equivalent
+        # FLOPs 2 * R * S * N * K against the bf16 tensor peak
+        for R in (512, 2048):
+            routes = [synth.routing_topk(R, E, S, seed=950 + R + j, device=dev)[0] for j in range(4)]
+            x = synth.normal_bf16((R, K), seed=13, device="cpu").to(dev)
+            y = torch.empty((R, S, N), dtype=torch.bfloat16, device=dev)
+            ws = wq.alloc_workspace(wq.wq_mxfp4_experts_shared_workspace(R, S, E, N, K), dev)
+
+            def call_g(i, copies=copies, routes=routes, x=x, y=y, ws=ws):
+                b_, s_ = copies[i % 2]
+                wq.wq_mxfp4_linear_experts_shared(x, b_, s_, routes[i % 4], y=y, workspace=ws, stream=stream)
+
+            us_g = time_rotating(call_g, 8, stream)
+            tf = 2.0 * R * S * N * K / (us_g * 1e-6) / 1e12
+            mx[f"grouped N={N} R={R}"] = {"us": round(us_g, 2), "tflops": round(tf, 1),
+                                          "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
+                                          "kernel": wq.wq_last_launch()}
     torch.cuda.synchronize()
     if int(st.item()) != 0:
         raise RuntimeError(f"quantize/pack device status {int(st.item())}")

@@ -245,6 +245,9 @@ WQ_API int wq_linear_int4_groups_noalloc(const void* x, int64_t M, int64_t K,
  *                          dependent launch, 2 without streaming weights before the
  *                          dependency wait
  *   WQ_TUNE_PREP_BLOCKS_PER_SM  blocks an SM the prepared-layout kernel is sized for (2)
+ *   WQ_TUNE_MX_GEMM_MIN_SLOTS   fewest routed slots (R * S) for which the MXFP4 expert
+ *                          products take the grouped tensor-core GEMM when the caller
+ *                          passes its workspace (default 512)
  * ------------------------------------------------------------------------------------ */
 enum {
   WQ_TUNE_GEMV_BLOCKS = 0,
@@ -254,7 +257,8 @@ enum {
   WQ_TUNE_GEMM_MIN_M = 4,
   WQ_TUNE_DECODE = 5,
   WQ_TUNE_PREP = 6,
-  WQ_TUNE_PREP_BLOCKS_PER_SM = 7
+  WQ_TUNE_PREP_BLOCKS_PER_SM = 7,
+  WQ_TUNE_MX_GEMM_MIN_SLOTS = 8
 };
 WQ_API int wq_set_tuning(int32_t knob, int64_t value);
 

@@ -22,7 +22,8 @@ WQ_OK, WQ_EINVAL, WQ_ESHAPE, WQ_EALIGN, WQ_ERANGE, WQ_EUNSUPPORTED, WQ_ECUDA, WQ
 WQ_DEV_NONFINITE, WQ_DEV_BAD_EXPERT, WQ_DEV_BAD_CODE, WQ_DEV_TIMEOUT, WQ_DEV_BAD_ORDER = 1, 2, 4, 8, 16
 WQ_SYM, WQ_SYM_U4, WQ_ASYM = 0, 1, 2
 (WQ_TUNE_GEMV_BLOCKS, WQ_TUNE_GEMV_CLUSTERS, WQ_TUNE_GEMV_PUSH, WQ_TUNE_GEMV_XSMEM,
- WQ_TUNE_GEMM_MIN_M, WQ_TUNE_DECODE, WQ_TUNE_PREP, WQ_TUNE_PREP_BLOCKS_PER_SM) = range(8)
+ WQ_TUNE_GEMM_MIN_M, WQ_TUNE_DECODE, WQ_TUNE_PREP, WQ_TUNE_PREP_BLOCKS_PER_SM,
+ WQ_TUNE_MX_GEMM_MIN_SLOTS) = range(9)
 
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
@@ -305,6 +306,12 @@ def wq_linear_int4_rows(x, packed, scale, bias=None, y=None, workspace=None, dev
     return y
 
 
+def _mxfp4_workspace(R, S, E, N, K, device):
+    # many routed slots: the grouped GEMM's scratch (routing tables and gathered rows)
+    n = wq_mxfp4_experts_shared_workspace(R, S, E, N, K)
+    return torch.empty(n, dtype=torch.uint8, device=device) if n else None
+
+
 def wq_mxfp4_experts_shared(x, blocks, scales, experts, y=None, workspace=None, dev_status=None,
                             stream=None):
     """x bf16 [R, 1, K] (or [R, K]); blocks u8 [E, N, K/32, 16]; scales u8 [E, N, K/32];
@@ -318,6 +325,8 @@ def wq_mxfp4_experts_shared(x, blocks, scales, experts, y=None, workspace=None, 
     S = experts.shape[1]
     if y is None:
         y = torch.empty((R, S, N), dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = _mxfp4_workspace(R, S, E, N, K, x.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = lib().wq_mxfp4_experts_shared(_ptr(x), R, K, _ptr(blocks), _ptr(scales), E, N, _ptr(experts), S,
                                        _ptr(y), _ptr(workspace), ws_bytes, _ptr(dev_status),
@@ -339,6 +348,8 @@ def wq_mxfp4_linear_experts_shared(x, blocks, scales, experts, y=None, workspace
     S = experts.shape[1]
     if y is None:
         y = torch.empty((R, S, N), dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = _mxfp4_workspace(R, S, E, N, K, x.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = lib().wq_mxfp4_linear_experts_shared(_ptr(x), R, K, _ptr(blocks), _ptr(scales), E, N, _ptr(experts),
                                               S, _ptr(y), _ptr(workspace), ws_bytes, _ptr(dev_status),

@@ -12,7 +12,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libwq.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["api.cu", "gemv.cu", "gemv_prep.cu", "gemv_mx.cu", "gemm_tc.cu", "quant.cu", "probe.cu"]
+SOURCES = ["api.cu", "gemv.cu", "gemv_prep.cu", "gemv_mx.cu", "gemm_tc.cu", "gemm_mx.cu", "quant.cu", "probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", INCLUDE]

@@ -404,16 +404,34 @@ WQ_API int wq_linear_int4_rows(const void* x, int64_t M, int64_t K, const int8_t
 // ------------------------------------------------------------------ MXFP4 experts
 WQ_API size_t wq_mxfp4_experts_shared_workspace(int64_t R, int64_t S, int64_t E, int64_t N,
                                                 int64_t K) {
-  (void)R; (void)S; (void)E; (void)N; (void)K;
-  return 0;
+  if (R <= 0 || S <= 0 || E <= 0 || N <= 0 || K <= 0) return 0;
+  // the grouped GEMM's routing tables and gathered rows (many routed slots); else none
+  return gemm_mx_ok(R, S, E, N, K, nullptr, nullptr, nullptr) ? gemm_mx_ws_bytes(R * S, E, K) : 0;
 }
 
 namespace {
-// The three MXFP4 expert products share one decode kernel: x_per_slot selects one input
-// row a slot; with y32 the slot results stay f32 (times sw) for the combine step.
+size_t round256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// The three MXFP4 expert products share the decode kernels: x_per_slot selects one input
+// row a slot; with y32 the slot results stay f32 (times sw) for the combine step.  With
+// many routed slots and the grouped GEMM's workspace (gws) they take the grouped GEMM.
 int run_mxfp4(const void* x, int64_t R, int64_t K, const uint8_t* blocks, const uint8_t* scales,
               int64_t E, int64_t N, const int32_t* experts, int64_t S, void* y, float* y32,
-              const float* sw, int x_per_slot, int32_t* dev_status, cudaStream_t s) {
+              const float* sw, int x_per_slot, void* gws, size_t gws_bytes, int32_t* dev_status,
+              cudaStream_t s) {
+  // a workspace too small for the grouped GEMM leaves the decode kernels (when they take
+  // the slot count)
+  if (gws != nullptr && !x_per_slot && gemm_mx_ok(R, S, E, N, K, x, blocks, scales) &&
+      gws_bytes >= gemm_mx_ws_bytes(R * S, E, K)) {
+    if (!aligned(gws, 16)) return WQ_EALIGN;
+    return launch_gemm_mx(static_cast<const __nv_bfloat16*>(x), R, S, blocks, scales, E, N, K,
+                          experts, static_cast<__nv_bfloat16*>(y), y32, sw, gws, dev_status, s) == cudaSuccess
+               ? WQ_OK
+               : WQ_ECUDA;
+  }
+  // the decode kernels' routing tables hold a bounded number of slots
+  if (!gemv_mxfp4_supported(R, S, E))
+    return gemm_mx_ok(R, S, E, N, K, x, blocks, scales) ? WQ_EWORKSPACE : WQ_EUNSUPPORTED;
   GemvParams p{};
   p.x = static_cast<const __nv_bfloat16*>(x);
   p.w = blocks;
@@ -437,7 +455,7 @@ int check_mxfp4(const void* x, int64_t R, int64_t K, const uint8_t* blocks, cons
   if (!x || !blocks || !scales || !experts || !y) return WQ_EINVAL;
   if (R <= 0 || K <= 0 || E <= 0 || N <= 0 || S <= 0) return WQ_EINVAL;
   if (K % 32 != 0) return WQ_ESHAPE;
-  if (!gemv_mxfp4_supported(R, S, E) || E * N > (1 << 30)) return WQ_EUNSUPPORTED;
+  if (E > 256 || E * N > (1 << 30) || K > (1 << 24) || R > (1 << 24) || S > (1 << 24)) return WQ_EUNSUPPORTED;
   if (!aligned(x, 16) || !aligned(blocks, 16) || !aligned(experts, 4) || !aligned(y, 2))
     return WQ_EALIGN;
   return WQ_OK;
@@ -448,7 +466,6 @@ WQ_API int wq_mxfp4_experts_shared(const void* x, int64_t R, int64_t K, const ui
                                    const uint8_t* scales, int64_t E, int64_t N,
                                    const int32_t* experts, int64_t S, void* y, void* workspace,
                                    size_t ws_bytes, int32_t* dev_status, wq_stream_t stream) {
-  (void)workspace; (void)ws_bytes;
   int st = check_mxfp4(x, R, K, blocks, scales, E, N, experts, S, y);
   if (st != WQ_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -456,7 +473,8 @@ WQ_API int wq_mxfp4_experts_shared(const void* x, int64_t R, int64_t K, const ui
   if (launch_zero_bad_slots(experts, R * S, E, N, static_cast<__nv_bfloat16*>(y), dev_status,
                             s) != cudaSuccess)
     return WQ_ECUDA;
-  return run_mxfp4(x, R, K, blocks, scales, E, N, experts, S, y, nullptr, nullptr, 0, dev_status, s);
+  return run_mxfp4(x, R, K, blocks, scales, E, N, experts, S, y, nullptr, nullptr, 0, workspace, ws_bytes,
+                   dev_status, s);
 }
 
 WQ_API int wq_mxfp4_linear_experts_shared(const void* x, int64_t R, int64_t K,
@@ -477,14 +495,17 @@ WQ_API int wq_mxfp4_experts(const void* x, int64_t R, int64_t K, const uint8_t* 
   if (launch_zero_bad_slots(experts, R * S, E, N, static_cast<__nv_bfloat16*>(y), dev_status,
                             s) != cudaSuccess)
     return WQ_ECUDA;
-  return run_mxfp4(x, R, K, blocks, scales, E, N, experts, S, y, nullptr, nullptr, 1, dev_status, s);
+  return run_mxfp4(x, R, K, blocks, scales, E, N, experts, S, y, nullptr, nullptr, 1, nullptr, 0, dev_status, s);
 }
 
 WQ_API size_t wq_mxfp4_combine_experts_workspace(int64_t R, int64_t S, int64_t E, int64_t N,
                                                  int64_t K) {
-  (void)E; (void)K;
   if (R <= 0 || S <= 0 || N <= 0) return 0;
-  return (size_t)R * (size_t)S * (size_t)N * 4;
+  const size_t y32 = (size_t)R * (size_t)S * (size_t)N * 4;
+  // many routed slots: the f32 slot results, then the grouped GEMM's workspace
+  if (E > 0 && K > 0 && gemm_mx_ok(R, S, E, N, K, nullptr, nullptr, nullptr))
+    return round256(y32) + gemm_mx_ws_bytes(R * S, E, K);
+  return y32;
 }
 
 WQ_API int wq_mxfp4_combine_experts(const void* x, int64_t R, int64_t K, const uint8_t* blocks,
@@ -495,14 +516,18 @@ WQ_API int wq_mxfp4_combine_experts(const void* x, int64_t R, int64_t K, const u
   int st = check_mxfp4(x, R, K, blocks, scales, E, N, experts, S, y);
   if (st != WQ_OK) return st;
   if (!weights || !workspace) return WQ_EINVAL;
-  if (ws_bytes < wq_mxfp4_combine_experts_workspace(R, S, E, N, K)) return WQ_EWORKSPACE;
+  if (ws_bytes < (size_t)R * (size_t)S * (size_t)N * 4) return WQ_EWORKSPACE;
   if (!aligned(weights, 4) || !aligned(workspace, 16)) return WQ_EALIGN;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // bad slots only set the status bit: the combine step skips them
   if (launch_zero_bad_slots(experts, R * S, E, N, nullptr, dev_status, s) != cudaSuccess)
     return WQ_ECUDA;
   float* y32 = static_cast<float*>(workspace);
-  st = run_mxfp4(x, R, K, blocks, scales, E, N, experts, S, nullptr, y32, weights, 0, dev_status, s);
+  const size_t y32_bytes = round256((size_t)R * (size_t)S * (size_t)N * 4);
+  const bool grouped = ws_bytes > y32_bytes && gemm_mx_ok(R, S, E, N, K, x, blocks, scales);
+  st = run_mxfp4(x, R, K, blocks, scales, E, N, experts, S, nullptr, y32, weights, 0,
+                 grouped ? static_cast<uint8_t*>(workspace) + y32_bytes : nullptr,
+                 grouped ? ws_bytes - y32_bytes : 0, dev_status, s);
   if (st != WQ_OK) return st;
   return launch_combine_slots(y32, experts, R, S, E, N, static_cast<__nv_bfloat16*>(y), s) ==
                  cudaSuccess

@@ -66,41 +66,6 @@ struct MxGeom {
   uint32_t off_sbuf, off_bars, off_x, off_route;  // offsets in dynamic shared memory
 };
 
-// bf16x2 a * b, rounded to nearest even
-__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-// (b & 0x80008000) | (a & 0x01C001C0): the sign of a code pair from b, exponent and
-// mantissa bits from a
-__device__ __forceinline__ uint32_t e2m1_pair_bits(uint32_t a, uint32_t b) {
-  uint32_t t, d;
-  asm("lop3.b32 %0, %1, 0x01C001C0, 0, 0xC0;" : "=r"(t) : "r"(a));
-  asm("lop3.b32 %0, %1, 0x80008000, %2, 0xEA;" : "=r"(d) : "r"(b), "r"(t));
-  return d;
-}
-// The eight codes of a word as four bf16x2 pairs (codes j and j + 4) of E2M1 * 2^-126,
-// each multiplied by s2 (bf16x2) and, for kTwo, then by s2b.
-template <bool kTwo>
-__device__ __forceinline__ void e2m1x8_scaled(uint32_t w, uint32_t s2, uint32_t s2b, uint32_t (&d)[4]) {
-  d[0] = e2m1_pair_bits(w << 6, w << 12);
-  d[1] = e2m1_pair_bits(w << 2, w << 8);
-  d[2] = e2m1_pair_bits(w >> 2, w << 4);
-  d[3] = e2m1_pair_bits(w >> 6, w);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    d[j] = mul_bf16x2(d[j], s2);
-    if constexpr (kTwo) d[j] = mul_bf16x2(d[j], s2b);
-  }
-}
-// bf16x2 of 2^(e - 1) (e <= 128), and of the E8M0 value 2^(e - 127) (NaN for 255)
-__device__ __forceinline__ uint32_t pow2_em1_bf16x2(uint32_t e) { return ((e + 126u) << 7) * 0x00010001u; }
-__device__ __forceinline__ uint32_t e8m0_bf16x2(uint32_t e) {
-  const uint32_t h = (e == 0u) ? 0x0040u : (e == 255u ? 0x7FC0u : (e << 7));
-  return h * 0x00010001u;
-}
-
 template <int kS, bool kXS>
 __global__ void __launch_bounds__(kMxThreads, 2)
     k_gemv_mx(const GemvParams p, const __grid_constant__ CUtensorMap wmap, const MxGeom g) {
