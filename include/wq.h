@@ -327,7 +327,15 @@ WQ_API size_t wq_linear_rows_workspace(int64_t M, int64_t N, int64_t K, int32_t 
  *   experts i32 [R, S]           (an index outside [0, E) gives a zero slot and sets
  *                                 WQ_DEV_BAD_EXPERT)
  *   y       bf16 [R, S, N]
- *   K % 32 == 0.  workspace: sized by wq_mxfp4_experts_shared_workspace(); same rules.
+ *   K % 32 == 0; at most 256 experts.
+ *   Regimes: up to 2048 routed slots (R * S) the decode kernels run, with no workspace.
+ *   From WQ_TUNE_MX_GEMM_MIN_SLOTS slots on (default 512) the grouped tensor-core GEMM
+ *   runs when the workspace is given: wq_mxfp4_experts_shared_workspace() bytes (0 below
+ *   the crossover), 16-byte aligned, holding the routing tables and the input rows
+ *   gathered in expert order.  It needs no zero-fill and holds scratch on return: do not
+ *   share it with the linears' split-K workspaces, which must stay zero-filled.  A
+ *   smaller workspace leaves the decode kernels; more than 2048 slots without it give
+ *   WQ_EWORKSPACE.
  * ------------------------------------------------------------------------------------ */
 WQ_API int wq_mxfp4_experts_shared(const void* x, int64_t R, int64_t K,
                                    const uint8_t* blocks, const uint8_t* scales,
@@ -355,12 +363,14 @@ WQ_API int wq_mxfp4_linear_experts_shared(const void* x, int64_t R, int64_t K,
  * multiplied from MXFP4, each slot its own input".
  *   y[r, s, n] = bf16( sum_k x[r, s, k] * W-hat_e[n, k] ),  e = experts[r, s]
  *   x bf16 [R, S, K] (one input row a slot); the other arguments as
- *   wq_mxfp4_experts_shared (no workspace).  An expert index outside [0, E) gives a zero
- *   slot and sets WQ_DEV_BAD_EXPERT.
+ *   wq_mxfp4_experts_shared, the workspace sized by wq_mxfp4_experts_workspace().  An
+ *   expert index outside [0, E) gives a zero slot and sets WQ_DEV_BAD_EXPERT.
  * ------------------------------------------------------------------------------------ */
 WQ_API int wq_mxfp4_experts(const void* x, int64_t R, int64_t K, const uint8_t* blocks,
                             const uint8_t* scales, int64_t E, int64_t N, const int32_t* experts,
-                            int64_t S, void* y, int32_t* dev_status, wq_stream_t stream);
+                            int64_t S, void* y, void* workspace, size_t ws_bytes,
+                            int32_t* dev_status, wq_stream_t stream);
+WQ_API size_t wq_mxfp4_experts_workspace(int64_t R, int64_t S, int64_t E, int64_t N, int64_t K);
 
 /* ------------------------------------------------------------------------------------
  * [Linnet] mxfp4_combine_experts(x, blocks, scales, experts, weights): "std.nn.moe::
@@ -370,9 +380,10 @@ WQ_API int wq_mxfp4_experts(const void* x, int64_t R, int64_t K, const uint8_t* 
  * a slot whose expert index lies outside [0, E) adding nothing (WQ_DEV_BAD_EXPERT set).
  *   x bf16 [R, K] (or [R, 1, K]); weights f32 [R, S] (the combine weights, e.g. a softmax
  *   over the row's routing logits); y bf16 [R, N].
- *   workspace: R * S * N f32 slot results (wq_mxfp4_combine_experts_workspace), 16-byte
- *   aligned, required (WQ_EINVAL if NULL, WQ_EWORKSPACE if too small); no zero-fill
- *   needed.  Each slot's f32 result is multiplied by its weight in the product kernel's
+ *   workspace: R * S * N f32 slot results, then (from the grouped GEMM's crossover on)
+ *   the grouped GEMM's scratch as for wq_mxfp4_experts_shared; sized by
+ *   wq_mxfp4_combine_experts_workspace(), 16-byte aligned, required (WQ_EINVAL if NULL,
+ *   WQ_EWORKSPACE if smaller than the slot results); no zero-fill needed.  Each slot's f32 result is multiplied by its weight in the product kernel's
  *   epilogue; a second small kernel adds a row's slots in slot order (deterministic) and
  *   rounds once to bf16.
  * ------------------------------------------------------------------------------------ */

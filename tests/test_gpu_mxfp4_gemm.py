@@ -5,9 +5,9 @@ mxfp4_linear_experts_shared "many rows (x: [R, In])", mxfp4_combine_experts).
 Cases: a slot count past the decode kernels' routing tables (4096), the gpt-oss gate/up
 shape at 2048 slots (sampled column ranges: the first and the last 256-wide tiles), a
 ragged N (not a multiple of 8) with K % 64 == 32, scales above 128 (two multiplies),
-every slot on one expert (many tiles of one segment) and a skewed routing (one-row
-segments), out-of-range expert indices, the combine form, the crossover knob, and the
-workspace rules.  Tolerance: |y_gpu - y_ref| <= 2e-3 * sum_k |x_k w_k| + 1 bf16 ulp(y_ref)."""
+every slot on one expert (many tiles of one segment; last tiles of 128 and 129 rows,
+one and two 128-row halves) and a skewed routing (one-row segments), out-of-range expert
+indices, the per-slot and combine forms, the crossover knob, and the workspace rules.  Tolerance: |y_gpu - y_ref| <= 2e-3 * sum_k |x_k w_k| + 1 bf16 ulp(y_ref)."""
 import numpy as np
 import pytest
 import torch
@@ -72,6 +72,8 @@ def _check_cols(y, x, blocks, scales, experts, N, n0, n1, what):
     (5, 200, 992, 300, 3, 110, 130, "topk", None),       # N ragged (scalar stores), K % 64 == 32
     (4, 640, 1536, 160, 4, 100, 200, "topk", None),      # scales above 128: two multiplies
     (6, 384, 1024, 700, 1, 118, 124, "one", None),       # one segment of 700 rows (3 tiles)
+    (6, 384, 1024, 640, 1, 118, 124, "one", None),       # last tile 128 rows: its first half only
+    (6, 384, 1024, 641, 1, 118, 124, "one", None),       # last tile 129 rows: both halves
     (12, 320, 1024, 600, 2, 118, 124, "skew", None),     # one large segment, one-row segments
     (32, 5760, 2880, 512, 4, 118, 124, "topk", ((0, 256), (5504, 5760))),  # gpt-oss gate/up
 ])
@@ -171,3 +173,25 @@ def test_grouped_gemm_workspace_rules(cuda_device):
     with pytest.raises(wq.WQError) as err:
         _run_shared(d, x2, blocks, scales, e2, N, workspace=small)
     assert err.value.status == wq.WQ_EWORKSPACE
+
+
+@pytest.mark.parametrize("E,N,K,R,S", [(8, 384, 1024, 300, 4), (16, 256, 768, 1024, 4)])
+def test_grouped_gemm_per_slot(cuda_device, E, N, K, R, S):
+    """mxfp4_experts: one input row a slot (x [R, S, K]), 1200 and 4096 slots."""
+    d = cuda_device
+    blocks, scales = _experts(E, N, K, seed=71 + R)
+    experts = _route(R, S, E, seed=72 + R)
+    experts[1, 2] = E + 3
+    x = synth.normal_bf16((R, S, K), seed=73 + R)
+    st = torch.zeros(1, dtype=torch.int32, device=d)
+    buf, y = guarded((R, S, N), torch.bfloat16, d)
+    ws = wq.alloc_workspace(wq.wq_mxfp4_experts_workspace(R, S, E, N, K), d)
+    wq.wq_mxfp4_experts(x.to(d), blocks.to(d), scales.to(d), experts.to(d), y=y, workspace=ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert guards_intact(buf)
+    assert "k_gemm_mx_tc" in wq.wq_last_launch(), wq.wq_last_launch()
+    assert int(st.item()) & wq.WQ_DEV_BAD_EXPERT
+    assert (y[1, 2].float() == 0).all()
+    yr, ad, bad = oracle.mxfp4_experts(bf16_bits(x), blocks.numpy(), scales.numpy(), experts.numpy(), N)
+    assert bad == 1
+    assert_within(y, yr, ad, f"per slot R={R} S={S}")

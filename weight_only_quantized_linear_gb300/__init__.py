@@ -57,7 +57,8 @@ SIGNATURES = {
     "wq_mxfp4_experts_shared_workspace": (_SZ, [_I64, _I64, _I64, _I64, _I64]),
     "wq_mxfp4_linear_experts_shared": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _I64, _P, _P,
                                                       _SZ, _P, _P]),
-    "wq_mxfp4_experts": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _I64, _P, _P, _P]),
+    "wq_mxfp4_experts": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _I64, _P, _P, _SZ, _P, _P]),
+    "wq_mxfp4_experts_workspace": (_SZ, [_I64, _I64, _I64, _I64, _I64]),
     "wq_mxfp4_combine_experts": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _I64, _P, _P, _P,
                                                 _SZ, _P, _P]),
     "wq_mxfp4_combine_experts_workspace": (_SZ, [_I64, _I64, _I64, _I64, _I64]),
@@ -358,7 +359,11 @@ def wq_mxfp4_linear_experts_shared(x, blocks, scales, experts, y=None, workspace
     return y
 
 
-def wq_mxfp4_experts(x, blocks, scales, experts, y=None, dev_status=None, stream=None):
+def wq_mxfp4_experts_workspace(R: int, S: int, E: int, N: int, K: int) -> int:
+    return int(lib().wq_mxfp4_experts_workspace(R, S, E, N, K))
+
+
+def wq_mxfp4_experts(x, blocks, scales, experts, y=None, workspace=None, dev_status=None, stream=None):
     """x bf16 [R, S, K] (one input a slot); blocks u8 [E, N, K/32, 16]; scales u8
     [E, N, K/32]; experts i32 [R, S].  Returns y bf16 [R, S, N]."""
     _need(x, torch.bfloat16, "x", 3)
@@ -371,8 +376,11 @@ def wq_mxfp4_experts(x, blocks, scales, experts, y=None, dev_status=None, stream
         raise ValueError("experts must be [R, S] with x [R, S, K]")
     if y is None:
         y = torch.empty((R, S, N), dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = _mxfp4_workspace(R, S, E, N, K, x.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = lib().wq_mxfp4_experts(_ptr(x), R, K, _ptr(blocks), _ptr(scales), E, N, _ptr(experts), S, _ptr(y),
-                                _ptr(dev_status), _stream(stream))
+                                _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream))
     _check(st, "wq_mxfp4_experts")
     return y
 

@@ -421,10 +421,10 @@ int run_mxfp4(const void* x, int64_t R, int64_t K, const uint8_t* blocks, const 
               cudaStream_t s) {
   // a workspace too small for the grouped GEMM leaves the decode kernels (when they take
   // the slot count)
-  if (gws != nullptr && !x_per_slot && gemm_mx_ok(R, S, E, N, K, x, blocks, scales) &&
+  if (gws != nullptr && gemm_mx_ok(R, S, E, N, K, x, blocks, scales) &&
       gws_bytes >= gemm_mx_ws_bytes(R * S, E, K)) {
     if (!aligned(gws, 16)) return WQ_EALIGN;
-    return launch_gemm_mx(static_cast<const __nv_bfloat16*>(x), R, S, blocks, scales, E, N, K,
+    return launch_gemm_mx(static_cast<const __nv_bfloat16*>(x), R, S, x_per_slot, blocks, scales, E, N, K,
                           experts, static_cast<__nv_bfloat16*>(y), y32, sw, gws, dev_status, s) == cudaSuccess
                ? WQ_OK
                : WQ_ECUDA;
@@ -486,16 +486,22 @@ WQ_API int wq_mxfp4_linear_experts_shared(const void* x, int64_t R, int64_t K,
                                  dev_status, stream);
 }
 
+WQ_API size_t wq_mxfp4_experts_workspace(int64_t R, int64_t S, int64_t E, int64_t N, int64_t K) {
+  return wq_mxfp4_experts_shared_workspace(R, S, E, N, K);
+}
+
 WQ_API int wq_mxfp4_experts(const void* x, int64_t R, int64_t K, const uint8_t* blocks,
                             const uint8_t* scales, int64_t E, int64_t N, const int32_t* experts,
-                            int64_t S, void* y, int32_t* dev_status, wq_stream_t stream) {
+                            int64_t S, void* y, void* workspace, size_t ws_bytes,
+                            int32_t* dev_status, wq_stream_t stream) {
   int st = check_mxfp4(x, R, K, blocks, scales, E, N, experts, S, y);
   if (st != WQ_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (launch_zero_bad_slots(experts, R * S, E, N, static_cast<__nv_bfloat16*>(y), dev_status,
                             s) != cudaSuccess)
     return WQ_ECUDA;
-  return run_mxfp4(x, R, K, blocks, scales, E, N, experts, S, y, nullptr, nullptr, 1, nullptr, 0, dev_status, s);
+  return run_mxfp4(x, R, K, blocks, scales, E, N, experts, S, y, nullptr, nullptr, 1, workspace, ws_bytes,
+                   dev_status, s);
 }
 
 WQ_API size_t wq_mxfp4_combine_experts_workspace(int64_t R, int64_t S, int64_t E, int64_t N,

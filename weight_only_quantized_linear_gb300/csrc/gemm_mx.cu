@@ -1,7 +1,7 @@
 // gemm_mx.cu -- MXFP4 experts with many routed rows (prefill and serving batches): a
 // grouped tcgen05 GEMM over the rows routed to each expert.
 //
-// "Quantization" (Linnet docs), format table: mxfp4_experts_shared and
+// "Quantization" (Linnet docs), format table: mxfp4_experts_shared, mxfp4_experts,
 // mxfp4_linear_experts_shared ("many rows (x: [R, In])"), mxfp4_combine_experts; "MXFP4
 // experts": the work grouped by expert.  The element is the same as in the decode kernels:
 // W-hat = bf16(E2M1 * 2^(scale - 127)), formed exactly (common.cuh, exact MXFP4 unpack).
@@ -12,7 +12,8 @@
 //                   sums of its 256-row tiles;
 //   2. k_gx_place   each valid slot takes a position in its expert's segment (the order
 //                   inside a segment is free: every output row is computed on its own);
-//   3. k_gx_gather  the shared input row of each position, copied in segment order with the
+//   3. k_gx_gather  the input row of each position (the routed row's shared input, or the
+//                   slot's own row for mxfp4_experts), copied in segment order with the
 //                   eight elements of every 16 bytes reordered (0, 4, 1, 5, 2, 6, 3, 7): the
 //                   pairing the unpack produces for the weights, so both MMA operands hold
 //                   the same permutation of k;
@@ -80,6 +81,7 @@ struct SharedGx {
   uint32_t tmem_base;
   int abort;
   int expert, m0, mend;
+  int halves;  // 128-row halves of the tile holding routed rows (1 or 2)
 };
 
 __global__ void __launch_bounds__(1024) k_gx_count(const int32_t* __restrict__ experts, int RS, int E,
@@ -124,7 +126,7 @@ __global__ void __launch_bounds__(256) k_gx_place(const int32_t* __restrict__ ex
 }
 
 __global__ void __launch_bounds__(256) k_gx_gather(const __nv_bfloat16* __restrict__ x, int64_t K, int64_t S,
-                                                   int E, const int32_t* __restrict__ hdr,
+                                                   int x_per_slot, int E, const int32_t* __restrict__ hdr,
                                                    const int32_t* __restrict__ sorted,
                                                    __nv_bfloat16* __restrict__ xg) {
   const int64_t k8n = K / 8;
@@ -133,7 +135,7 @@ __global__ void __launch_bounds__(256) k_gx_gather(const __nv_bfloat16* __restri
        idx += (int64_t)gridDim.x * blockDim.x) {
     const int64_t pos = idx / k8n, k8 = idx - pos * k8n;
     const int slot = sorted[pos];
-    const int64_t row = slot / S;  // the routed row the slot belongs to
+    const int64_t row = x_per_slot ? slot : slot / S;  // the slot's own row, or its routed row's
     const uint4 v = ld_global_nc_v4(x + row * K + k8 * 8);
     const uint4 o = make_uint4(__byte_perm(v.x, v.z, 0x5410), __byte_perm(v.x, v.z, 0x7632),
                                __byte_perm(v.y, v.w, 0x5410), __byte_perm(v.y, v.w, 0x7632));
@@ -174,11 +176,15 @@ __global__ void __launch_bounds__(kGxThreads, 1)
     sh->expert = e;
     sh->m0 = (e >= 0) ? seg[e] + (t - tst[e]) * kGxBM : 0;
     sh->mend = (e >= 0) ? seg[e + 1] : 0;
+    sh->halves = (sh->mend - sh->m0 > kGxBM / 2) ? 2 : 1;
   }
   __syncthreads();
   const int expert = sh->expert;
   if (expert < 0) return;  // past the last tile (the grid is sized for the worst case)
   const int64_t m0 = sh->m0, mend = sh->mend;
+  // a tile with at most 128 routed rows (small segments, a segment's last tile) loads,
+  // multiplies and stores only its first half: one accumulator instead of two
+  const int halves = sh->halves;
   const int64_t n0 = (int64_t)blockIdx.y * kGxBN;
   const int nk = (int)((K + kGxBK - 1) / kGxBK);  // K % 64 == 32: the last step's second block reads zeros
 
@@ -214,8 +220,10 @@ __global__ void __launch_bounds__(kGxThreads, 1)
           break;
         }
         if (*reinterpret_cast<volatile int*>(&sh->abort)) break;
-        mbar_arrive_expect_tx(&sh->full_tma[s], kGxABytes + kGxPBytes);
-        tma_load_2d(stage_a(s), &xmap, &sh->full_tma[s], kb * kGxBK, (int32_t)m0, pol);
+        mbar_arrive_expect_tx(&sh->full_tma[s], halves * (kGxABytes / 2) + kGxPBytes);
+        for (int h = 0; h < halves; ++h)
+          tma_load_2d(stage_a(s) + h * (kGxABytes / 2), &xmap, &sh->full_tma[s], kb * kGxBK,
+                      (int32_t)(m0 + h * (kGxBM / 2)), pol);
         tma_load_2d(stage_p(s), &wmap, &sh->full_tma[s], kb * (kGxBK / 2), wrow, pol);
         issued = kb + 1;
       }
@@ -238,8 +246,7 @@ __global__ void __launch_bounds__(kGxThreads, 1)
         tc_fence_after();
         const uint32_t a_base = smem_u32(stage_a(s));
         const uint32_t b_base = smem_u32(stage_b(s));
-#pragma unroll
-        for (int acc = 0; acc < 2; ++acc) {
+        for (int acc = 0; acc < halves; ++acc) {
 #pragma unroll
           for (int kk = 0; kk < kGxBK / 16; ++kk) {
             const uint64_t ad = umma_desc_sw128(a_base + acc * (128 * 128) + kk * 32);
@@ -319,11 +326,12 @@ __global__ void __launch_bounds__(kGxThreads, 1)
     tc_fence_after();
     const int q = warp & 3;
     const int acc = (warp - 2) >> 2;
+    const int chunks = (acc < halves) ? kGxBN / 32 : 0;  // the second half of a half tile: no rows
     const int64_t m = m0 + acc * 128 + q * 32 + lane;  // position in the sorted slot list
     const int slot = (m < mend) ? p.sorted[m] : -1;
     const float wgt = (slot >= 0 && p.sw) ? __ldg(p.sw + slot) : 1.0f;
 #pragma unroll 1
-    for (int ch = 0; ch < kGxBN / 32; ++ch) {
+    for (int ch = 0; ch < chunks; ++ch) {
       uint32_t r[32];
       tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + acc * kGxBN + ch * 32, r);
       const int64_t nb = n0 + ch * 32;
@@ -390,7 +398,7 @@ bool gemm_mx_ok(int64_t R, int64_t S, int64_t E, int64_t N, int64_t K, const voi
 
 size_t gemm_mx_ws_bytes(int64_t RS, int64_t E, int64_t K) { return gx_layout(RS, E, K).total; }
 
-cudaError_t launch_gemm_mx(const __nv_bfloat16* x, int64_t R, int64_t S, const uint8_t* blocks,
+cudaError_t launch_gemm_mx(const __nv_bfloat16* x, int64_t R, int64_t S, int x_per_slot, const uint8_t* blocks,
                            const uint8_t* scales, int64_t E, int64_t N, int64_t K, const int32_t* experts,
                            __nv_bfloat16* y, float* y32, const float* sw, void* workspace,
                            int32_t* dev_status, cudaStream_t stream) {
@@ -402,7 +410,7 @@ cudaError_t launch_gemm_mx(const __nv_bfloat16* x, int64_t R, int64_t S, const u
   __nv_bfloat16* xg = reinterpret_cast<__nv_bfloat16*>(ws + L.xg);
   CUtensorMap xmap, wmap;
   if (!encode_tensor_map_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xg, (uint64_t)K, (uint64_t)RS,
-                            (uint64_t)K * 2, kGxBK, kGxBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+                            (uint64_t)K * 2, kGxBK, kGxBM / 2, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tensor_map_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t*>(blocks),
                             (uint64_t)K / 2, (uint64_t)(E * N), (uint64_t)K / 2, kGxBK / 2, kGxBN,
                             CU_TENSOR_MAP_SWIZZLE_32B))
@@ -424,7 +432,7 @@ cudaError_t launch_gemm_mx(const __nv_bfloat16* x, int64_t R, int64_t S, const u
   k_gx_place<<<(unsigned)((RS + 255) / 256), 256, 0, stream>>>(experts, (int)RS, (int)E, hdr, sorted);
   const int64_t pieces = RS * (K / 8);
   const unsigned gblocks = (unsigned)std::min<int64_t>((pieces + 255) / 256, 4096);
-  k_gx_gather<<<gblocks, 256, 0, stream>>>(x, K, S, (int)E, hdr, sorted, xg);
+  k_gx_gather<<<gblocks, 256, 0, stream>>>(x, K, S, x_per_slot, (int)E, hdr, sorted, xg);
   // tiles: at most RS / 256 + one more for every expert with rows
   const int64_t tiles_max = (RS + kGxBM - 1) / kGxBM + std::min<int64_t>(E, RS);
   const dim3 grid((unsigned)tiles_max, (unsigned)((N + kGxBN - 1) / kGxBN));

@@ -91,13 +91,13 @@ cudaError_t launch_gemv_mx(const GemvParams& p, int num_sms, cudaStream_t stream
 // holds for R * S >= the crossover (WQ_TUNE_MX_GEMM_MIN_SLOTS, default 512), at most 256
 // experts, K % 32 == 0 and 16-byte aligned x, codes and scales; the workspace
 // (gemm_mx_ws_bytes, 256-byte aligned) holds the routing tables and the gathered rows.
-// x: the shared input [R, K]; y: bf16 [R * S, N]; or, with y32 set, f32 [R * S, N] slot
-// results times sw[slot].
+// x: the shared input [R, K], or with x_per_slot one row a slot [R * S, K]; y: bf16
+// [R * S, N]; or, with y32 set, f32 [R * S, N] slot results times sw[slot].
 // Slots with an expert index outside [0, E) are not written.
 bool gemm_mx_ok(int64_t R, int64_t S, int64_t E, int64_t N, int64_t K, const void* x, const void* blocks,
                 const void* scales);
 size_t gemm_mx_ws_bytes(int64_t RS, int64_t E, int64_t K);
-cudaError_t launch_gemm_mx(const __nv_bfloat16* x, int64_t R, int64_t S, const uint8_t* blocks,
+cudaError_t launch_gemm_mx(const __nv_bfloat16* x, int64_t R, int64_t S, int x_per_slot, const uint8_t* blocks,
                            const uint8_t* scales, int64_t E, int64_t N, int64_t K, const int32_t* experts,
                            __nv_bfloat16* y, float* y32, const float* sw, void* workspace,
                            int32_t* dev_status, cudaStream_t stream);
