@@ -108,6 +108,11 @@ def test_grouped_gemm_bad_experts(cuda_device):
     for r, s in ((3, 0), (77, 2), (199, 3)):
         assert (y[r, s].float() == 0).all()
     assert _check_cols(y, x, blocks, scales, experts, N, 0, N, "bad experts") == 3
+    # no valid slot at all: only the zero-row tiles run
+    y0, st0 = _run_shared(d, x, blocks, scales, torch.full((R, S), -2, dtype=torch.int32), N)
+    assert "k_gemm_mx_tc" in wq.wq_last_launch()
+    assert st0 & wq.WQ_DEV_BAD_EXPERT
+    assert (y0.float() == 0).all()
 
 
 def test_grouped_gemm_combine(cuda_device):

@@ -432,6 +432,11 @@ int run_mxfp4(const void* x, int64_t R, int64_t K, const uint8_t* blocks, const 
   // the decode kernels' routing tables hold a bounded number of slots
   if (!gemv_mxfp4_supported(R, S, E))
     return gemm_mx_ok(R, S, E, N, K, x, blocks, scales) ? WQ_EWORKSPACE : WQ_EUNSUPPORTED;
+  // slots whose expert index is out of range: zero rows of y (the combine step skips
+  // them: only the status bit), by a small kernel ahead of the decode kernel
+  if (launch_zero_bad_slots(experts, R * S, E, N, static_cast<__nv_bfloat16*>(y), dev_status, s) !=
+      cudaSuccess)
+    return WQ_ECUDA;
   GemvParams p{};
   p.x = static_cast<const __nv_bfloat16*>(x);
   p.w = blocks;
@@ -469,10 +474,6 @@ WQ_API int wq_mxfp4_experts_shared(const void* x, int64_t R, int64_t K, const ui
   int st = check_mxfp4(x, R, K, blocks, scales, E, N, experts, S, y);
   if (st != WQ_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // slots whose expert index is out of range are zero-filled by a small kernel
-  if (launch_zero_bad_slots(experts, R * S, E, N, static_cast<__nv_bfloat16*>(y), dev_status,
-                            s) != cudaSuccess)
-    return WQ_ECUDA;
   return run_mxfp4(x, R, K, blocks, scales, E, N, experts, S, y, nullptr, nullptr, 0, workspace, ws_bytes,
                    dev_status, s);
 }
@@ -497,9 +498,6 @@ WQ_API int wq_mxfp4_experts(const void* x, int64_t R, int64_t K, const uint8_t* 
   int st = check_mxfp4(x, R, K, blocks, scales, E, N, experts, S, y);
   if (st != WQ_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (launch_zero_bad_slots(experts, R * S, E, N, static_cast<__nv_bfloat16*>(y), dev_status,
-                            s) != cudaSuccess)
-    return WQ_ECUDA;
   return run_mxfp4(x, R, K, blocks, scales, E, N, experts, S, y, nullptr, nullptr, 1, workspace, ws_bytes,
                    dev_status, s);
 }
@@ -525,9 +523,6 @@ WQ_API int wq_mxfp4_combine_experts(const void* x, int64_t R, int64_t K, const u
   if (ws_bytes < (size_t)R * (size_t)S * (size_t)N * 4) return WQ_EWORKSPACE;
   if (!aligned(weights, 4) || !aligned(workspace, 16)) return WQ_EALIGN;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // bad slots only set the status bit: the combine step skips them
-  if (launch_zero_bad_slots(experts, R * S, E, N, nullptr, dev_status, s) != cudaSuccess)
-    return WQ_ECUDA;
   float* y32 = static_cast<float*>(workspace);
   const size_t y32_bytes = round256((size_t)R * (size_t)S * (size_t)N * 4);
   const bool grouped = ws_bytes > y32_bytes && gemm_mx_ok(R, S, E, N, K, x, blocks, scales);

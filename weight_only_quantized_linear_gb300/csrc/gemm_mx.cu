@@ -6,23 +6,24 @@
 // experts": the work grouped by expert.  The element is the same as in the decode kernels:
 // W-hat = bf16(E2M1 * 2^(scale - 127)), formed exactly (common.cuh, exact MXFP4 unpack).
 //
-// Steps (one stream, four launches):
-//   1. k_gx_count   per-expert row counts of the routed slots, their exclusive prefix
-//                   sums (each expert's segment of the sorted slot list) and the prefix
-//                   sums of its 256-row tiles;
-//   2. k_gx_place   each valid slot takes a position in its expert's segment (the order
-//                   inside a segment is free: every output row is computed on its own);
-//   3. k_gx_gather  the input row of each position (the routed row's shared input, or the
+// Steps (one stream, three launches):
+//   1. k_gx_route   (one block) per-expert counts of the routed slots, each expert's
+//                   segment of the sorted slot list and the prefix sums of its 256-row
+//                   tiles, then each slot's position in its segment; slots with an expert
+//                   index outside [0, E) form a last segment (WQ_DEV_BAD_EXPERT);
+//   2. k_gx_gather  the input row of each position (the routed row's shared input, or the
 //                   slot's own row for mxfp4_experts), copied in segment order with the
 //                   eight elements of every 16 bytes reordered (0, 4, 1, 5, 2, 6, 3, 7): the
 //                   pairing the unpack produces for the weights, so both MMA operands hold
 //                   the same permutation of k;
-//   4. k_gemm_mx_tc one block a (256-row tile of one expert's segment, 256 weight rows):
+//   3. k_gemm_mx_tc one block a (256-row tile of one expert's segment, 256 weight rows):
 //                   warp 0 loads the activation tile and the expert's packed codes by TMA,
 //                   warps 2..9 unpack the codes into the canonical 128-byte-swizzled bf16
 //                   tile, one thread of warp 1 issues tcgen05.mma into two 128 x 256 TMEM
-//                   accumulators; the epilogue writes each row to its slot of y (bf16), or
-//                   its f32 result times the slot's weight to the combine workspace.
+//                   accumulators (one for a tile of at most 128 rows); the epilogue writes
+//                   each row to its slot of y (bf16), or its f32 result times the slot's
+//                   weight to the combine workspace.  Tiles of the last segment write zero
+//                   rows to y and multiply nothing.
 // Every wait is bounded; a timeout records WQ_DEV_TIMEOUT and the block winds down.
 #include <algorithm>
 #include <atomic>
@@ -47,8 +48,8 @@ constexpr int kGxStageBytes = kGxABytes + kGxBBytes + kGxPBytes;
 constexpr int kGxMaxExperts = 256;
 constexpr int kGxMinSlots = 512;  // routed slots from which the GEMM takes over (default)
 
-// Workspace: header [4][E + 1] i32 (counts, segment starts, tile starts, fill counters),
-// sorted slots [RS] i32, gathered activations [RS, K] bf16; sections 256-byte aligned.
+// Workspace: header [2][E + 2] i32 (segment starts, tile starts), sorted slots [RS] i32,
+// gathered activations [RS, K] bf16; sections 256-byte aligned.
 // Tiles that reach past the gathered rows read zeros (the tensor map's bounds).
 struct GxLayout {
   size_t sorted, xg, total;
@@ -56,14 +57,14 @@ struct GxLayout {
 GxLayout gx_layout(int64_t RS, int64_t E, int64_t K) {
   auto al = [](size_t v) { return (v + 255) & ~size_t(255); };
   GxLayout L;
-  L.sorted = al(4 * 4 * (size_t)(E + 1));
+  L.sorted = al(2 * 4 * (size_t)(E + 2));
   L.xg = L.sorted + al(4 * (size_t)RS);
   L.total = L.xg + al((size_t)RS * (size_t)K * 2);
   return L;
 }
 
 struct GxParams {
-  const int32_t* hdr;      // [4][E + 1]
+  const int32_t* hdr;      // [2][E + 2]: segment starts, tile starts (segment E: bad slots)
   const int32_t* sorted;   // [RS]
   const uint8_t* escale;   // [E, N, K/32]
   int64_t E, N, K;
@@ -84,45 +85,41 @@ struct SharedGx {
   int halves;  // 128-row halves of the tile holding routed rows (1 or 2)
 };
 
-__global__ void __launch_bounds__(1024) k_gx_count(const int32_t* __restrict__ experts, int RS, int E,
-                                                   int32_t* __restrict__ hdr) {
-  __shared__ int s_cnt[kGxMaxExperts];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+// One block: the routed slots' segments.  Segment e < E holds the slots routed to expert
+// e; segment E the slots whose expert index lies outside [0, E) (zero rows, no product).
+// The header gets the segment starts and the prefix sums of each segment's 256-row tiles;
+// each slot then takes a position in its segment (the order inside a segment is free:
+// every output row is computed on its own).
+__global__ void __launch_bounds__(1024) k_gx_route(const int32_t* __restrict__ experts, int RS, int E,
+                                                   int32_t* __restrict__ hdr, int32_t* __restrict__ sorted,
+                                                   int32_t* __restrict__ dev_status) {
+  __shared__ int s_cnt[kGxMaxExperts + 1];
+  __shared__ int s_fill[kGxMaxExperts + 1];
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) s_cnt[e] = 0;
   __syncthreads();
-  for (int i = threadIdx.x; i < RS; i += blockDim.x) {
+  auto seg_of = [&](int i) {
     const int e = experts[i];
-    if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
-  }
+    return (e >= 0 && e < E) ? e : E;
+  };
+  for (int i = threadIdx.x; i < RS; i += blockDim.x) atomicAdd(&s_cnt[seg_of(i)], 1);
   __syncthreads();
   if (threadIdx.x == 0) {
-    int32_t* cnt = hdr;
-    int32_t* seg = hdr + (E + 1);
-    int32_t* tst = hdr + 2 * (E + 1);
-    int32_t* fill = hdr + 3 * (E + 1);
+    int32_t* const seg = hdr;
+    int32_t* const tst = hdr + (E + 2);
     int run = 0, truns = 0;
-    for (int e = 0; e < E; ++e) {
-      cnt[e] = s_cnt[e];
+    for (int e = 0; e <= E; ++e) {
       seg[e] = run;
       tst[e] = truns;
-      fill[e] = 0;
+      s_fill[e] = run;
       run += s_cnt[e];
       truns += (s_cnt[e] + kGxBM - 1) / kGxBM;
     }
-    cnt[E] = 0;
-    seg[E] = run;
-    tst[E] = truns;
-    fill[E] = 0;
+    seg[E + 1] = run;
+    tst[E + 1] = truns;
+    if (s_cnt[E] > 0) set_dev_status(dev_status, WQ_DEV_BAD_EXPERT);
   }
-}
-
-__global__ void __launch_bounds__(256) k_gx_place(const int32_t* __restrict__ experts, int RS, int E,
-                                                  int32_t* __restrict__ hdr, int32_t* __restrict__ sorted) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= RS) return;
-  const int e = experts[i];
-  if (e < 0 || e >= E) return;
-  const int pos = hdr[(E + 1) + e] + atomicAdd(&hdr[3 * (E + 1) + e], 1);
-  sorted[pos] = i;
+  __syncthreads();
+  for (int i = threadIdx.x; i < RS; i += blockDim.x) sorted[atomicAdd(&s_fill[seg_of(i)], 1)] = i;
 }
 
 __global__ void __launch_bounds__(256) k_gx_gather(const __nv_bfloat16* __restrict__ x, int64_t K, int64_t S,
@@ -130,7 +127,7 @@ __global__ void __launch_bounds__(256) k_gx_gather(const __nv_bfloat16* __restri
                                                    const int32_t* __restrict__ sorted,
                                                    __nv_bfloat16* __restrict__ xg) {
   const int64_t k8n = K / 8;
-  const int64_t total = (int64_t)hdr[(E + 1) + E] * k8n;  // valid slots x 16-byte pieces
+  const int64_t total = (int64_t)hdr[E] * k8n;  // routed slots (segments 0 .. E - 1) x 16-byte pieces
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += (int64_t)gridDim.x * blockDim.x) {
     const int64_t pos = idx / k8n, k8 = idx - pos * k8n;
@@ -158,15 +155,15 @@ __global__ void __launch_bounds__(kGxThreads, 1)
   const int lane = threadIdx.x & 31;
   const int E = (int)p.E;
   const int64_t N = p.N, K = p.K;
-  const int32_t* const seg = p.hdr + (E + 1);
-  const int32_t* const tst = p.hdr + 2 * (E + 1);
+  const int32_t* const seg = p.hdr;
+  const int32_t* const tst = p.hdr + (E + 2);
 
-  // this block's tile: the expert whose tile range holds blockIdx.x
+  // this block's tile: the segment whose tile range holds blockIdx.x
   if (threadIdx.x == 0) {
     const int t = (int)blockIdx.x;
     int e = -1;
-    if (t < tst[E]) {
-      int lo = 0, hi = E - 1;  // largest e with tst[e] <= t (and a tile of its own)
+    if (t < tst[E + 1]) {
+      int lo = 0, hi = E;  // largest e with tst[e] <= t (and a tile of its own)
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
         if (tst[mid] <= t) lo = mid; else hi = mid - 1;
@@ -182,6 +179,20 @@ __global__ void __launch_bounds__(kGxThreads, 1)
   const int expert = sh->expert;
   if (expert < 0) return;  // past the last tile (the grid is sized for the worst case)
   const int64_t m0 = sh->m0, mend = sh->mend;
+  if (expert == E) {
+    // slots with an expert index outside [0, E): zero rows of y (the combine form skips
+    // them); no product
+    if (p.y != nullptr) {
+      const int64_t n0z = (int64_t)blockIdx.y * kGxBN;
+      const int64_t nz = imin64(N - n0z, kGxBN);
+      const int64_t rows = imin64(mend - m0, kGxBM);
+      for (int64_t i = threadIdx.x; i < rows * nz; i += blockDim.x) {
+        const int64_t r = i / nz;
+        p.y[(int64_t)p.sorted[m0 + r] * N + n0z + (i - r * nz)] = __float2bfloat16_rn(0.0f);
+      }
+    }
+    return;
+  }
   // a tile with at most 128 routed rows (small segments, a segment's last tile) loads,
   // multiplies and stores only its first half: one accumulator instead of two
   const int halves = sh->halves;
@@ -209,7 +220,10 @@ __global__ void __launch_bounds__(kGxThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&xmap);
       tma_prefetch_desc(&wmap);
+      // the gathered rows are reread for every 256 weight rows: kept in L2; an expert's
+      // codes serve only the blocks of its segment, which run together: streamed
       const uint64_t pol = l2_policy_evict_last();
+      const uint64_t pol_w = l2_policy_evict_first();
       const int32_t wrow = (int32_t)((int64_t)expert * N + n0);
       int issued = 0;
       for (int kb = 0; kb < nk; ++kb) {
@@ -224,7 +238,7 @@ __global__ void __launch_bounds__(kGxThreads, 1)
         for (int h = 0; h < halves; ++h)
           tma_load_2d(stage_a(s) + h * (kGxABytes / 2), &xmap, &sh->full_tma[s], kb * kGxBK,
                       (int32_t)(m0 + h * (kGxBM / 2)), pol);
-        tma_load_2d(stage_p(s), &wmap, &sh->full_tma[s], kb * (kGxBK / 2), wrow, pol);
+        tma_load_2d(stage_p(s), &wmap, &sh->full_tma[s], kb * (kGxBK / 2), wrow, pol_w);
         issued = kb + 1;
       }
       for (int kb = std::max(0, issued - kGxStages); kb < issued; ++kb)
@@ -428,16 +442,15 @@ cudaError_t launch_gemm_mx(const __nv_bfloat16* x, int64_t R, int64_t S, int x_p
     if (e != cudaSuccess) return e;
     attr_set.fetch_or(bit, std::memory_order_release);
   }
-  k_gx_count<<<1, 1024, 0, stream>>>(experts, (int)RS, (int)E, hdr);
-  k_gx_place<<<(unsigned)((RS + 255) / 256), 256, 0, stream>>>(experts, (int)RS, (int)E, hdr, sorted);
+  k_gx_route<<<1, 1024, 0, stream>>>(experts, (int)RS, (int)E, hdr, sorted, dev_status);
   const int64_t pieces = RS * (K / 8);
   const unsigned gblocks = (unsigned)std::min<int64_t>((pieces + 255) / 256, 4096);
   k_gx_gather<<<gblocks, 256, 0, stream>>>(x, K, S, x_per_slot, (int)E, hdr, sorted, xg);
-  // tiles: at most RS / 256 + one more for every expert with rows
-  const int64_t tiles_max = (RS + kGxBM - 1) / kGxBM + std::min<int64_t>(E, RS);
+  // tiles: at most RS / 256 + one more for every segment with rows
+  const int64_t tiles_max = (RS + kGxBM - 1) / kGxBM + std::min<int64_t>(E + 1, RS);
   const dim3 grid((unsigned)tiles_max, (unsigned)((N + kGxBN - 1) / kGxBN));
   GxParams gp{hdr, sorted, scales, E, N, K, y, y32, sw, dev_status};
-  note_launch("k_gemm_mx_tc<grouped by expert,tile=256x256> grid=%ux%u (k_gx_count, k_gx_place, k_gx_gather first)",
+  note_launch("k_gemm_mx_tc<grouped by expert,tile=256x256> grid=%ux%u (k_gx_route, k_gx_gather first)",
               grid.x, grid.y);
   k_gemm_mx_tc<<<grid, kGxThreads, smem, stream>>>(xmap, wmap, gp);
   return cudaGetLastError();
