@@ -76,6 +76,7 @@ def _check_cols(y, x, blocks, scales, experts, N, n0, n1, what):
     (6, 384, 1024, 641, 1, 118, 124, "one", None),       # last tile 129 rows: both halves
     (12, 320, 1024, 600, 2, 118, 124, "skew", None),     # one large segment, one-row segments
     (32, 5760, 2880, 512, 4, 118, 124, "topk", ((0, 256), (5504, 5760))),  # gpt-oss gate/up
+    (32, 2880, 2880, 2048, 4, 118, 124, "topk", ((0, 256), (2816, 2880))),  # gpt-oss down, 8192 slots
 ])
 def test_grouped_gemm_matches_oracle(cuda_device, E, N, K, R, S, elo, ehi, kind, cols):
     d = cuda_device
@@ -200,3 +201,17 @@ def test_grouped_gemm_per_slot(cuda_device, E, N, K, R, S):
     yr, ad, bad = oracle.mxfp4_experts(bf16_bits(x), blocks.numpy(), scales.numpy(), experts.numpy(), N)
     assert bad == 1
     assert_within(y, yr, ad, f"per slot R={R} S={S}")
+
+
+@pytest.mark.parametrize("E,N,K,R,S", [(3, 16, 64, 40, 2), (2, 24, 96, 30, 2), (4, 8, 32, 50, 3)])
+def test_grouped_gemm_small_shapes(cuda_device, tune, E, N, K, R, S):
+    """Shapes smaller than a TMA box (K of one or two blocks, E * N under 256 rows, fewer
+    routed rows than a half tile), forced onto the grouped GEMM by the crossover knob."""
+    d = cuda_device
+    tune(wq.WQ_TUNE_MX_GEMM_MIN_SLOTS, 1)
+    blocks, scales = _experts(E, N, K, seed=81 + K)
+    experts = _route(R, S, E, seed=82 + K)
+    x = synth.normal_bf16((R, K), seed=83 + K)
+    y, st = _run_shared(d, x, blocks, scales, experts, N)
+    assert st == 0 and "k_gemm_mx_tc" in wq.wq_last_launch(), wq.wq_last_launch()
+    assert _check_cols(y, x, blocks, scales, experts, N, 0, N, f"E={E} N={N} K={K}") == 0
