@@ -13,9 +13,10 @@
 // weights, a step 128 bytes of each of the tile's rows (256 codes).  As in the cluster
 // kernel of the affine formats (gemv.cu), a cluster takes a contiguous range of items,
 // its warps split the range's (item, step) units evenly, and tiles cut between warps are
-// finished inside the cluster through distributed shared memory.  Clusters of two CTAs:
-// the loop is bound by instruction issue, so every SM should hold the same two CTAs
-// (clusters of eight left a fifth of the SMs with one, measured on GB300).
+// finished inside the cluster through distributed shared memory.  One CTA of 16 warps an
+// SM, in clusters of two: with two CTAs of 8 warps an SM, the warps of one CTA ran ahead
+// of the other's (by 15 us of a 79 us launch at eight routed rows, measured on GB300), and
+// the SM finished the slower CTA's work with half its warps.
 //
 // Loads: each warp streams its units through its own ring of stages filled by TMA (a
 // {128 bytes, 16 rows} box of the experts' codes stacked as [E * N rows, K / 2 bytes],
@@ -42,10 +43,10 @@
 namespace wq {
 namespace {
 
-constexpr int kMxWarps = 8;
+constexpr int kMxWarps = 16;
 constexpr int kMxThreads = kMxWarps * 32;
 constexpr int kMxCluster = 2;     // CTAs a cluster
-constexpr int kMxClWarpsLog2 = 4; // log2(warps a cluster)
+constexpr int kMxClWarpsLog2 = 5; // log2(warps a cluster)
 static_assert(kMxCluster * kMxWarps == (1 << kMxClWarpsLog2), "warps a cluster: a power of two");
 constexpr int kMxRows = 16;        // weight rows a tile
 constexpr int kMxStepBytes = 128;  // code bytes of a row a step (256 codes)
@@ -67,7 +68,7 @@ struct MxGeom {
 };
 
 template <int kS, bool kXS>
-__global__ void __launch_bounds__(kMxThreads, 2)
+__global__ void __launch_bounds__(kMxThreads, 1)
     k_gemv_mx(const GemvParams p, const __grid_constant__ CUtensorMap wmap, const MxGeom g) {
   // partial D fragments of cut tiles: [warp][first / last segment][lane][4]
   __shared__ __align__(16) float s_part[kMxWarps][2][32][4];
@@ -490,8 +491,10 @@ MxLayout mx_layout(const GemvParams& p, int kS, uint32_t xrows, uint32_t xstride
 }
 
 constexpr size_t kMxSmemPerSM = 228 * 1024;
+constexpr size_t kMxSmemPerBlock = 227 * 1024;
 constexpr size_t kMxStaticBytes = (size_t)kMxWarps * 2 * 32 * 4 * sizeof(float);
-bool mx_fits(size_t dyn) { return 2 * (dyn + kMxStaticBytes + 1024) <= kMxSmemPerSM; }
+// one block an SM: dynamic + static + the 1 KB the driver reserves
+bool mx_fits(size_t dyn) { return dyn + kMxStaticBytes + 1024 <= kMxSmemPerSM && dyn + kMxStaticBytes <= kMxSmemPerBlock; }
 
 template <int kS, bool kXS>
 cudaError_t launch_mx_t(const GemvParams& p, const CUtensorMap& wmap, const MxLayout& L, int num_sms,
@@ -502,7 +505,7 @@ cudaError_t launch_mx_t(const GemvParams& p, const CUtensorMap& wmap, const MxLa
   const uint64_t bit = 1ull << dev;
   if (!(smem_set.load(std::memory_order_acquire) & bit)) {
     const cudaError_t e = cudaFuncSetAttribute(k_gemv_mx<kS, kXS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)(kMxSmemPerSM / 2));
+                                               (int)(kMxSmemPerBlock - kMxStaticBytes));
     if (e != cudaSuccess) return e;
     smem_set.fetch_or(bit, std::memory_order_acq_rel);
   }
@@ -523,9 +526,9 @@ cudaError_t launch_mx_t(const GemvParams& p, const CUtensorMap& wmap, const MxLa
   int active = 0;
   if (cudaOccupancyMaxActiveClusters(&active, k_gemv_mx<kS, kXS>, &cfg) != cudaSuccess || active <= 0) {
     (void)cudaGetLastError();
-    active = num_sms * 2 / kMxCluster;
+    active = num_sms / kMxCluster;
   }
-  // every co-resident cluster (two CTAs on every SM), but at least two steps a warp on
+  // every co-resident cluster (one CTA on every SM), but at least two steps a warp on
   // average for the largest routing the launch can see
   const int64_t units_max = (int64_t)L.g.pairs_max * L.g.tiles * L.g.spt;
   int64_t clusters = std::min<int64_t>((int64_t)active,
@@ -558,7 +561,7 @@ cudaError_t launch_gemv_mx(const GemvParams& p, int num_sms, cudaStream_t stream
                             (uint64_t)(p.K / 2), (uint64_t)(p.E * p.N), (uint64_t)(p.K / 2),
                             kMxStepBytes, kMxRows, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  // activations staged when two blocks an SM still fit (a four-, else three-stage ring)
+  // activations staged when the block still fits (a four-, else three-stage ring)
   const uint32_t xrows = (uint32_t)(p.x_per_slot ? p.M * p.S : p.M);
   const uint32_t kpad = (uint32_t)(((p.K + 255) / 256) * 256);
   const uint32_t xstride = kpad * 2 + (xrows > 1 ? 64u : 0u);
