@@ -406,6 +406,7 @@ bool gemm_mx_ok(int64_t R, int64_t S, int64_t E, int64_t N, int64_t K, const voi
   const int64_t RS = R * S;
   if (RS < gemm_mx_min_slots() || E > kGxMaxExperts || K % 32 != 0 || K < 32 || N < 1) return false;
   if (RS >= (int64_t(1) << 30) || E * N >= (int64_t(1) << 31)) return false;
+  if ((N + kGxBN - 1) / kGxBN > 65535) return false;  // column blocks: the grid's y extent
   return ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(blocks) |
            reinterpret_cast<uintptr_t>(scales)) & 15) == 0;
 }
