@@ -77,6 +77,7 @@ def _check_cols(y, x, blocks, scales, experts, N, n0, n1, what):
     (12, 320, 1024, 600, 2, 118, 124, "skew", None),     # one large segment, one-row segments
     (32, 5760, 2880, 512, 4, 118, 124, "topk", ((0, 256), (5504, 5760))),  # gpt-oss gate/up
     (32, 2880, 2880, 2048, 4, 118, 124, "topk", ((0, 256), (2816, 2880))),  # gpt-oss down, 8192 slots
+    (32, 200, 992, 100, 6, 100, 200, "topk", None),      # 32 experts: ragged N, K % 64 == 32, scales > 128
 ])
 def test_grouped_gemm_matches_oracle(cuda_device, E, N, K, R, S, elo, ehi, kind, cols):
     d = cuda_device
