@@ -216,3 +216,36 @@ def test_grouped_gemm_small_shapes(cuda_device, tune, E, N, K, R, S):
     y, st = _run_shared(d, x, blocks, scales, experts, N)
     assert st == 0 and "k_gemm_mx_tc" in wq.wq_last_launch(), wq.wq_last_launch()
     assert _check_cols(y, x, blocks, scales, experts, N, 0, N, f"E={E} N={N} K={K}") == 0
+
+
+def test_grouped_gemm_in_cuda_graph(cuda_device):
+    """Captured once in a CUDA graph, replayed with new routings and inputs written into
+    the same buffers: the launch shape does not depend on the routing (the grid is sized
+    for the worst case), so every replay matches the oracle."""
+    d = cuda_device
+    E, N, K, R, S = 16, 512, 1024, 256, 4
+    blocks, scales = _experts(E, N, K, seed=91)
+    bd, sd = blocks.to(d), scales.to(d)
+    x_buf = torch.empty((R, K), dtype=torch.bfloat16, device=d)
+    e_buf = torch.empty((R, S), dtype=torch.int32, device=d)
+    y = torch.empty((R, S, N), dtype=torch.bfloat16, device=d)
+    ws = wq.alloc_workspace(wq.wq_mxfp4_experts_shared_workspace(R, S, E, N, K), d)
+    routes = [_route(R, S, E, seed=92), _route(R, S, E, seed=93, kind="skew"), _route(R, S, E, seed=94, kind="one")]
+    xs = [synth.normal_bf16((R, K), seed=95 + i) for i in range(3)]
+    x_buf.copy_(xs[0])
+    e_buf.copy_(routes[0])
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        wq.wq_mxfp4_linear_experts_shared(x_buf, bd, sd, e_buf, y=y, workspace=ws, stream=stream)  # warm-up
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            wq.wq_mxfp4_linear_experts_shared(x_buf, bd, sd, e_buf, y=y, workspace=ws, stream=stream)
+    assert "k_gemm_mx_tc" in wq.wq_last_launch()
+    for i in (1, 2, 0):
+        x_buf.copy_(xs[i])
+        e_buf.copy_(routes[i])
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert _check_cols(y, xs[i], blocks, scales, routes[i], N, 0, N, f"replay {i}") == 0
