@@ -432,11 +432,8 @@ int run_mxfp4(const void* x, int64_t R, int64_t K, const uint8_t* blocks, const 
   // the decode kernels' routing tables hold a bounded number of slots
   if (!gemv_mxfp4_supported(R, S, E))
     return gemm_mx_ok(R, S, E, N, K, x, blocks, scales) ? WQ_EWORKSPACE : WQ_EUNSUPPORTED;
-  // slots whose expert index is out of range: zero rows of y (the combine step skips
-  // them: only the status bit), by a small kernel ahead of the decode kernel
-  if (launch_zero_bad_slots(experts, R * S, E, N, static_cast<__nv_bfloat16*>(y), dev_status, s) !=
-      cudaSuccess)
-    return WQ_ECUDA;
+  // slots whose expert index is out of range get zero rows of y (the combine step skips
+  // them: only the status bit) from the decode path itself
   GemvParams p{};
   p.x = static_cast<const __nv_bfloat16*>(x);
   p.w = blocks;

@@ -1380,11 +1380,16 @@ cudaError_t launch_f(const GemvParams& p, int64_t rows, int grid, int num_sms, c
     if (fact_ok(F, p) && tuning(kKnobDecode) != 2)
       return rows <= 8 ? launch_fact<F, 1>(p, num_sms, stream) : launch_fact<F, 2>(p, num_sms, stream);
   } else {
-    // MXFP4: the TMA-ring cluster kernel (gemv_mx.cu) where its shape rules hold
+    // MXFP4: the TMA-ring cluster kernel (gemv_mx.cu) where its shape rules hold; it
+    // writes the zero rows of out-of-range slots itself
     if (gemv_mx_ok(p) && tuning(kKnobDecode) != 2) {
       const cudaError_t e = launch_gemv_mx(p, num_sms, stream);
       if (e != cudaErrorNotSupported) return e;
     }
+    // the exact kernel leaves them to a small kernel (y NULL in the combine form: only
+    // the status bit)
+    const cudaError_t e = launch_zero_bad_slots(p.experts, p.M * p.S, p.E, p.N, p.y, p.dev_status, stream);
+    if (e != cudaSuccess) return e;
   }
   GemvParams q = p;
   if (q.order != nullptr) {  // the exact kernel reads activations from global memory

@@ -33,6 +33,9 @@
 // range) and the NaN scale 255 take two multiplies (by 2^126, then by the E8M0 value).
 // Codes j and j + 4 of a word form one bf16x2 pair, the pairing of the group-wise kernels,
 // so activations are staged in the same permuted order.
+//
+// Slots whose expert index lies outside [0, E) are left out of the routing tables; the
+// grid writes their rows of y as zeros and sets WQ_DEV_BAD_EXPERT.
 
 #include <algorithm>
 #include <atomic>
@@ -216,6 +219,19 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     }
   }
   __syncthreads();
+
+  // slots whose expert index lies outside [0, E): the status bit, and zero rows of y
+  // (the combine form only skips them), spread over the grid
+  if (ebase[E - 1] + ecnt[E - 1] < RS) {
+    if (blockIdx.x == 0 && tid == 0) set_dev_status(p.dev_status, WQ_DEV_BAD_EXPERT);
+    if (p.y != nullptr) {
+      const int64_t total = (int64_t)RS * N;
+      for (int64_t i = (int64_t)blockIdx.x * kMxThreads + tid; i < total; i += (int64_t)gridDim.x * kMxThreads) {
+        const int e = eidx[i / N];
+        if (e < 0 || e >= E) p.y[i] = __float2bfloat16_rn(0.0f);
+      }
+    }
+  }
 
   const uint32_t npairs = (uint32_t)route[0];
   const uint32_t items = npairs * tiles;
