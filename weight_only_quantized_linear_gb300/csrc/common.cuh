@@ -467,7 +467,6 @@ __device__ __forceinline__ void nib8_minus_zero(uint32_t w, uint32_t zc, uint32_
   }
 }
 
-
 // ------------------------------------------------------------------ exact MXFP4 unpack
 // A code (s, e1 e0, m) with its sign in bf16 bit 15 and e1 e0 m in bits 8..6 is the bf16
 // E2M1 * 2^-126 (the 0 / 0.5 codes as subnormals); one packed bf16 multiply by 2^(e - 1)
