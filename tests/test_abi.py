@@ -88,3 +88,37 @@ def test_host_validation_without_a_device(lib):
     assert lib.wq_mxfp4_experts_shared(fake, 1, 48, fake, fake, 4, 8, fake, 2, fake, None, 0, None,
                                        None) == wq.WQ_ESHAPE
     assert lib.wq_dequantize_int4_groups(fake, fake, fake, 4, 96, 64, fake, None) == wq.WQ_ESHAPE
+
+
+def test_mxfp4_workspace_queries_and_regimes(lib):
+    """The MXFP4 workspace rules, on the host: no workspace below the grouped GEMM's
+    crossover (512 routed rows by default), above it segment and tile starts
+    [2, E + 2] i32, the sorted slots [R * S] i32 and the gathered rows [R * S, K] bf16,
+    each rounded to 256 bytes; the combine form adds its f32 slot results in front."""
+    al = lambda v: (v + 255) // 256 * 256
+    gemm_ws = lambda RS, E, K: al(2 * 4 * (E + 2)) + al(4 * RS) + al(RS * K * 2)
+    E, N, K, S = 32, 5760, 2880, 4
+    assert lib.wq_mxfp4_experts_shared_workspace(127, S, E, N, K) == 0            # 508 slots
+    assert lib.wq_mxfp4_combine_experts_workspace(127, S, E, N, K) == 127 * S * N * 4
+    for R in (128, 2048):
+        need = gemm_ws(R * S, E, K)
+        assert lib.wq_mxfp4_experts_shared_workspace(R, S, E, N, K) == need
+        assert lib.wq_mxfp4_experts_workspace(R, S, E, N, K) == need
+        assert lib.wq_mxfp4_combine_experts_workspace(R, S, E, N, K) == al(R * S * N * 4) + need
+    # outside the GEMM's rules: none (K not a multiple of 32, more than 256 experts)
+    assert lib.wq_mxfp4_experts_shared_workspace(2048, S, E, N, 2880 + 16) == 0
+    assert lib.wq_mxfp4_experts_shared_workspace(2048, S, 300, N, K) == 0
+    # the crossover knob moves the regime, and 0 restores it
+    try:
+        assert lib.wq_set_tuning(wq.WQ_TUNE_MX_GEMM_MIN_SLOTS, 1) == wq.WQ_OK
+        assert lib.wq_mxfp4_experts_shared_workspace(2, S, E, N, K) == gemm_ws(2 * S, E, K)
+    finally:
+        lib.wq_set_tuning(wq.WQ_TUNE_MX_GEMM_MIN_SLOTS, 0)
+    assert lib.wq_mxfp4_experts_shared_workspace(2, S, E, N, K) == 0
+    # more routed rows than the decode kernels' tables hold, and no workspace: refused
+    # before any launch
+    fake = ctypes.c_void_p(0x10000)
+    assert lib.wq_mxfp4_experts_shared(fake, 1024, 64, fake, fake, 4, 16, fake, 4, fake, None, 0, None,
+                                       None) == wq.WQ_EWORKSPACE
+    assert lib.wq_mxfp4_experts(fake, 1024, 64, fake, fake, 4, 16, fake, 4, fake, None, 0, None,
+                                None) == wq.WQ_EWORKSPACE
